@@ -1,0 +1,707 @@
+#!/usr/bin/env python3
+"""Benchmark of the multi-LoRA adapter hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Metric: adapted tokens/s per LoRA layer -- tokens that pass through one
+adapted projection per second (a step over L projections of T tokens counts
+T * L).  Rank 0 prints one JSON line.
+
+Workloads (``--workload``; default ``decode_bgmv``):
+  decode_bgmv         256 decode tokens, ids uniform over 32 adapters, 4096->4096,
+                      rank 16, bf16.  A step is one decode pass through 32
+                      layers' adapted q projection: 32 lora_bgmv launches, each
+                      layer with its own x, y and adapter pages.
+  prefill_sgmv        8192 tokens in 16 Zipf(1.2) segments; a step is shrink +
+                      expand on q, k, v, o.
+  encoder_mixed_rank  16384 tokens (128 x 128), 1024 adapters of ranks 8..64,
+                      a step is shrink + expand on all 48 projections.
+  fused_layer         4 x 1024 prefill + 512 decode tokens; a step is
+                      lora_layer_forward on q, k, v, o (base GEMM + adapter).
+
+Each step is captured once in a CUDA graph and replayed; the timed region is
+bracketed by a barrier and a device synchronise on both sides and measured
+with CUDA events on the launching stream; the step time is the max over
+ranks.  Every step's working set exceeds L2 (per-layer buffers), so no flush
+is needed.  Under torchrun every rank runs its own batch (weak scaling, no
+collective on the data path).
+
+``--impl reference`` times the CPU oracle (the plain fp64 definition) on the
+host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from segmented_gathered_rank_gb300 import accounting as A  # noqa: E402
+from segmented_gathered_rank_gb300 import inputs as I  # noqa: E402
+
+METRIC = "adapted tokens/s per LoRA layer on 1 GB300; % of HBM / tensor-core roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES_NOMINAL = 129e6
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """ncu DRAM bytes per launch recorded for a kernel, with the source digest
+    they were taken at (a changed kernel reports null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "segmented_gathered_rank_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, n), "rb") as f:
+                h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU; none for N = 1)
+# ----------------------------------------------------------------------------
+class Dist:
+    def __init__(self, backend: str | None = None):
+        import torch
+        import torch.distributed as dist
+        self.dist = dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.on = self.world > 1
+        if self.on and not dist.is_initialized():
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            if backend is None:
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+        self.backend = dist.get_backend() if self.on else None
+
+    def _tensor(self, v):
+        import torch
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        return torch.tensor([float(v)], dtype=torch.float64, device=dev)
+
+    def barrier(self):
+        if self.on:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.on:
+            return float(v)
+        t = self._tensor(v)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v: float) -> float:
+        if not self.on:
+            return float(v)
+        t = self._tensor(v)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.on and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
+def aggregate(units_per_rank_step: float, steps: int, max_seconds: float, dist: Dist):
+    """Whole-job throughput: units every rank processed / the slowest rank's time."""
+    total_units = dist.sum(units_per_rank_step * steps)
+    t = dist.max(max_seconds)
+    return total_units / t if t > 0 else 0.0, t
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------
+# Workloads
+# ----------------------------------------------------------------------------
+class Runner:
+    """One workload: device state, the step, and its accounting."""
+    name = ""
+    units_per_step = 0
+    dominant = {}          # name, bound, work_per_launch, launches_per_step, unit
+
+    def step(self, stream=None):
+        raise NotImplementedError
+
+    def dominant_step(self, stream=None):
+        """Launches of the dominant kernel for one step (default: the step)."""
+        self.step(stream)
+
+
+class DecodeBGMV(Runner):
+    name = "decode_bgmv"
+
+    def __init__(self, layers: int = 32, seed: int = 0):
+        import torch
+        from segmented_gathered_rank_gb300 import harness as H
+        from segmented_gathered_rank_gb300 import lora as L
+        self.L, self.H, self.torch = L, H, torch
+        self.layers = layers
+        w = self.w = I.decode_bgmv(seed=seed, layers=layers)
+        self.T, self.h = w.T, w.matrices[0].h_in
+        self.pool = H.DevicePool(w, matrices=[0], layers=layers)
+        self.x = torch.stack([H.to_device(w.x(0, l), w.dtype) for l in range(layers)])
+        self.y0_host = np.stack([w.y0(0, l) for l in range(layers)])
+        self.y = torch.stack([H.to_device(self.y0_host[l], w.dtype) for l in range(layers)])
+        self.tok = H.int_tensor(w.token_adapter)
+        self.units_per_step = self.T * layers
+        per = A.bgmv_bytes(w.token_adapter, w.ranks, self.h, self.h, 2)
+        self.dominant = dict(name="lora_bgmv (bgmv kernel)", bound="hbm", work_per_launch=per,
+                             launches_per_step=layers, unit="GB/s")
+        self.working_set = layers * (per + 0)
+        self.config = {"workload": "decode_bgmv: 256 decode tokens, ids ~ U{0..31}, q_proj 4096->4096, rank 16, "
+                                   f"bf16; step = {layers} layers x lora_bgmv",
+                       "tokens": self.T, "layers": layers, "h_in": self.h, "h_out": self.h, "rank": 16,
+                       "adapters": 32, "distinct_adapters": int(len(w.used_adapters())),
+                       "l2": f"inputs larger than L2: {layers} layers' x, y and adapter pages "
+                             f"({self.working_set / 1e6:.0f} MB) rotated per step"}
+
+    def step(self, stream=None):
+        for l in range(self.layers):
+            self.L.lora_bgmv(self.pool.handle, l, self.x[l], self.y[l], self.tok, self.T, stream)
+
+    # end to end: inputs from pinned host memory, result back to pinned memory
+    def e2e_setup(self):
+        torch = self.torch
+        self.x_h = self.x.cpu().pin_memory()
+        self.y0_h = self.y.cpu().pin_memory()
+        self.tok_h = self.tok.cpu().pin_memory()
+        self.out_h = torch.empty_like(self.y0_h).pin_memory()
+        self.h2d = self.x_h.numel() * 2 + self.y0_h.numel() * 2 + self.tok_h.numel() * 4
+        self.d2h = self.out_h.numel() * 2
+
+    def e2e_step(self):
+        self.x.copy_(self.x_h, non_blocking=True)
+        self.y.copy_(self.y0_h, non_blocking=True)
+        self.tok.copy_(self.tok_h, non_blocking=True)
+        self.step()
+        self.out_h.copy_(self.y, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle
+        units, t_total, layers_done = 0, 0.0, 0
+        l = 0
+        cache = self.__dict__.setdefault("_cpu_cache", {})
+        while True:
+            w = self.w
+            key = l % 4
+            if key not in cache:
+                cache[key] = (oracle.adapters_for(w, 0, layer=key), w.x(0, key).astype(np.float64))
+            ad, x = cache[key]
+            t0 = time.perf_counter()
+            oracle.layer(x, None, w.token_adapter, ad, self.h)
+            t_total += time.perf_counter() - t0
+            units += self.T
+            layers_done += 1
+            l += 1
+            if t_total >= budget_s or layers_done >= self.layers * 8:
+                break
+        return units / t_total, f"{layers_done} layers x {self.T} tokens (oracle.layer, no base), {t_total:.1f} s"
+
+
+class PrefillSGMV(Runner):
+    name = "prefill_sgmv"
+
+    def __init__(self, seed: int = 0):
+        import torch
+        from segmented_gathered_rank_gb300 import harness as H
+        from segmented_gathered_rank_gb300 import lora as L
+        self.L, self.H, self.torch = L, H, torch
+        w = self.w = I.prefill_sgmv(seed=seed)
+        self.T = w.T
+        self.pool = H.DevicePool(w)
+        self.ss, self.sa = H.int_tensor(w.seg_starts), H.int_tensor(w.seg_adapter)
+        self.x = {0: H.to_device(w.x(0), w.dtype), 3: H.to_device(w.x(3), w.dtype)}
+        self.y = [H.to_device(w.y0(m), w.dtype) for m in range(4)]
+        self.v = [torch.zeros((w.T, w.max_rank), dtype=torch.float32, device="cuda") for _ in range(4)]
+        self.units_per_step = self.T * 4
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
+        self.shrink_b = [A.shrink_bytes(tok, w.ranks, mt.h_in, 2, w.max_rank) for mt in w.matrices]
+        self.expand_b = [A.expand_bytes(tok, w.ranks, mt.h_out, 2) for mt in w.matrices]
+        self.dominant = dict(name="lora_sgmv_expand", bound="hbm", work_per_launch=sum(self.expand_b) / 4,
+                             launches_per_step=4, unit="GB/s")
+        ws = sum(self.shrink_b) + sum(self.expand_b)
+        self.config = {"workload": "prefill_sgmv: 8192 tokens in 16 Zipf(1.2) segments (cap 2048), 16 of 64 "
+                                   "adapters, q/o 4096->4096, k/v 4096->1024, rank 16, bf16; step = shrink+expand "
+                                   "on q,k,v,o",
+                       "tokens": self.T, "segments": w.S, "rank": 16,
+                       "l2": f"inputs larger than L2: {ws / 1e6:.0f} MB touched per step"}
+
+    def _x(self, m):
+        return self.x[0] if m < 3 else self.x[3]
+
+    def step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(4):
+            L.lora_sgmv_shrink(self.pool.handle, m, self._x(m), self.v[m], w.max_rank, self.ss, self.sa, w.S, w.T,
+                               stream)
+            L.lora_sgmv_expand(self.pool.handle, m, self.v[m], w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T,
+                               stream)
+
+    def dominant_step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(4):
+            L.lora_sgmv_expand(self.pool.handle, m, self.v[m], w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T,
+                               stream)
+
+    def e2e_setup(self):
+        self.x_h = {k: v.cpu().pin_memory() for k, v in self.x.items()}
+        self.y_h = [y.cpu().pin_memory() for y in self.y]
+        self.out_h = [self.torch.empty_like(y).pin_memory() for y in self.y_h]
+        self.h2d = sum(t.numel() * 2 for t in self.x_h.values()) + sum(t.numel() * 2 for t in self.y_h)
+        self.d2h = sum(t.numel() * 2 for t in self.out_h)
+
+    def e2e_step(self):
+        for k in self.x:
+            self.x[k].copy_(self.x_h[k], non_blocking=True)
+        for y, yh in zip(self.y, self.y_h):
+            y.copy_(yh, non_blocking=True)
+        self.step()
+        for o, y in zip(self.out_h, self.y):
+            o.copy_(y, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle
+        w = self.w
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+        rng = np.random.default_rng(0)
+        units, t_total, n = 0, 0.0, 0
+        xs = {0: w.x(0).astype(np.float64), 3: w.x(3).astype(np.float64)}
+        ads = [oracle.adapters_for(w, m) for m in range(4)]
+        while True:
+            m = n % 4
+            rows = np.sort(rng.choice(w.T, 1024, replace=False)).astype(np.int32)
+            t0 = time.perf_counter()
+            oracle.layer(xs[0 if m < 3 else 3], None, tok, ads[m], w.matrices[m].h_out, rows=rows)
+            t_total += time.perf_counter() - t0
+            units += len(rows)
+            n += 1
+            if t_total >= budget_s or n >= 64:
+                break
+        return units / t_total, f"{n} projections x 1024 sampled tokens (oracle.layer, no base), {t_total:.1f} s"
+
+
+class EncoderMixedRank(Runner):
+    name = "encoder_mixed_rank"
+
+    def __init__(self, seed: int = 0):
+        import torch
+        from segmented_gathered_rank_gb300 import harness as H
+        from segmented_gathered_rank_gb300 import lora as L
+        self.L, self.H, self.torch = L, H, torch
+        w = self.w = I.encoder_mixed_rank(seed=seed)
+        self.T, self.M = w.T, len(w.matrices)
+        used = set(w.used_adapters().tolist())
+        self.pool = H.DevicePool(w, filler=lambda a: a not in used)
+        self.ss, self.sa = H.int_tensor(w.seg_starts), H.int_tensor(w.seg_adapter)
+        self.x = [H.to_device(w.x(m), w.dtype) for m in range(self.M)]
+        self.y = [H.to_device(w.y0(m), w.dtype) for m in range(self.M)]
+        self.v = torch.zeros((w.T, w.max_rank), dtype=torch.float32, device="cuda")
+        self.units_per_step = self.T * self.M
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
+        eb = A.expand_bytes(tok, w.ranks, 768, 2)
+        sb = A.shrink_bytes(tok, w.ranks, 768, 2, w.max_rank)
+        self.dominant = dict(name="lora_sgmv_expand", bound="hbm", work_per_launch=eb, launches_per_step=self.M,
+                             unit="GB/s")
+        self.config = {"workload": "encoder_mixed_rank: 128 sequences x 128 tokens, Zipf(1.1) ids over 1024 "
+                                   "adapters with ranks {8,16,32,64} (p .4/.3/.2/.1), 12 layers x q/k/v/o 768->768, "
+                                   "pages of 768, bf16; step = shrink+expand on 48 projections",
+                       "tokens": self.T, "matrices": self.M, "distinct_adapters": len(used),
+                       "pool_gb": round(self.pool.n_pages * 768 * 2 / 1e9, 2),
+                       "l2": f"inputs larger than L2: {self.M * (eb + sb) / 1e6:.0f} MB touched per step"}
+
+    def step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(self.M):
+            L.lora_sgmv_shrink(self.pool.handle, m, self.x[m], self.v, w.max_rank, self.ss, self.sa, w.S, w.T, stream)
+            L.lora_sgmv_expand(self.pool.handle, m, self.v, w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T, stream)
+
+    def dominant_step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(self.M):
+            L.lora_sgmv_expand(self.pool.handle, m, self.v, w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T, stream)
+
+    def e2e_setup(self):
+        self.x_h = [t.cpu().pin_memory() for t in self.x]
+        self.y_h = [t.cpu().pin_memory() for t in self.y]
+        self.out_h = [self.torch.empty_like(t).pin_memory() for t in self.y_h]
+        self.h2d = sum(t.numel() * 2 for t in self.x_h + self.y_h)
+        self.d2h = sum(t.numel() * 2 for t in self.out_h)
+
+    def e2e_step(self):
+        for d, h in zip(self.x + self.y, self.x_h + self.y_h):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        for o, y in zip(self.out_h, self.y):
+            o.copy_(y, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle
+        w = self.w
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+        rng = np.random.default_rng(0)
+        units, t_total, n = 0, 0.0, 0
+        cache = self.__dict__.setdefault("_cpu_cache", {})
+        while True:
+            m = n % 4
+            if m not in cache:
+                cache[m] = (oracle.adapters_for(w, m), w.x(m).astype(np.float64))
+            ad, x = cache[m]
+            rows = np.sort(rng.choice(w.T, 2048, replace=False)).astype(np.int32)
+            t0 = time.perf_counter()
+            oracle.layer(x, None, tok, ad, 768, rows=rows)
+            t_total += time.perf_counter() - t0
+            units += len(rows)
+            n += 1
+            if t_total >= budget_s or n >= 48:
+                break
+        return units / t_total, f"{n} projections x 2048 sampled tokens (oracle.layer, no base), {t_total:.1f} s"
+
+
+class FusedLayer(Runner):
+    name = "fused_layer"
+
+    def __init__(self, seed: int = 0):
+        import torch
+        from segmented_gathered_rank_gb300 import harness as H
+        from segmented_gathered_rank_gb300 import lora as L
+        self.L, self.H, self.torch = L, H, torch
+        w = self.w = I.fused_layer(seed=seed)
+        self.T = w.T
+        self.pool = H.DevicePool(w)
+        self.ss, self.sa = H.int_tensor(w.seg_starts), H.int_tensor(w.seg_adapter)
+        self.x = {0: H.to_device(w.x(0), w.dtype), 3: H.to_device(w.x(3), w.dtype)}
+        self.W = [H.to_device(w.W(m), w.dtype) for m in range(4)]
+        self.y = [torch.empty((w.T, mt.h_out), dtype=torch.bfloat16, device="cuda") for mt in w.matrices]
+        self.ws_bytes = max(L.lora_layer_forward_workspace_size(self.pool.handle, m, w.S, w.T) for m in range(4))
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.units_per_step = self.T * 4
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
+        self.flops = [A.layer_flops(tok, w.ranks, mt.h_in, mt.h_out) for mt in w.matrices]
+        self.dominant = dict(name="lora_layer_forward (base GEMM + adapter term)", bound="tensor",
+                             work_per_launch=sum(self.flops) / 4, launches_per_step=4, unit="TFLOP/s")
+        self.config = {"workload": "fused_layer: 4x1024 prefill + 512 decode tokens, Llama-3-8B q/k/v/o "
+                                   "(4096->4096/1024/1024/4096), 128 adapters Zipf(1.0), rank 16 (adapter 0 rank "
+                                   "128), bf16; step = lora_layer_forward on q,k,v,o",
+                       "tokens": self.T, "flops_per_step": int(sum(self.flops)),
+                       "l2": "inputs larger than L2: W 84 MB + x 75 MB + y 94 MB per step"}
+
+    def _x(self, m):
+        return self.x[0] if m < 3 else self.x[3]
+
+    def step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(4):
+            L.lora_layer_forward(self.pool.handle, m, self._x(m), self.W[m], self.y[m], self.ss, self.sa, w.S, w.T,
+                                 self.ws, self.ws_bytes, stream)
+
+    def e2e_setup(self):
+        self.x_h = {k: v.cpu().pin_memory() for k, v in self.x.items()}
+        self.out_h = [self.torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in self.y]
+        self.h2d = sum(t.numel() * 2 for t in self.x_h.values())
+        self.d2h = sum(t.numel() * 2 for t in self.out_h)
+
+    def e2e_step(self):
+        for k in self.x:
+            self.x[k].copy_(self.x_h[k], non_blocking=True)
+        self.step()
+        for o, y in zip(self.out_h, self.y):
+            o.copy_(y, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle
+        w = self.w
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+        rng = np.random.default_rng(0)
+        xs = {0: w.x(0).astype(np.float64), 3: w.x(3).astype(np.float64)}
+        units, t_total, n = 0, 0.0, 0
+        cache = self.__dict__.setdefault("_cpu_cache", {})
+        while True:
+            m = n % 4
+            if m not in cache:
+                cache[m] = (oracle.adapters_for(w, m), w.W(m).astype(np.float64))
+            ad, W = cache[m]
+            rows = np.sort(rng.choice(w.T, 32, replace=False)).astype(np.int32)
+            t0 = time.perf_counter()
+            oracle.layer(xs[0 if m < 3 else 3], W, tok, ad, w.matrices[m].h_out, rows=rows)
+            t_total += time.perf_counter() - t0
+            units += len(rows)
+            n += 1
+            if t_total >= budget_s or n >= 16:
+                break
+        return units / t_total, f"{n} projections x 32 sampled tokens (oracle.layer with base), {t_total:.1f} s"
+
+
+RUNNERS = {"decode_bgmv": DecodeBGMV, "prefill_sgmv": PrefillSGMV, "encoder_mixed_rank": EncoderMixedRank,
+           "fused_layer": FusedLayer}
+
+DTYPE = "bf16"
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args, dist: Dist):
+    """The CPU oracle, timed on the host cores, on bounded samples of the workload."""
+    if dist.rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    cls = RUNNERS[args.workload]
+    r = cls.__new__(cls)          # only the generator side: no device state
+    r.w = {"decode_bgmv": lambda: I.decode_bgmv(layers=32), "prefill_sgmv": I.prefill_sgmv,
+           "encoder_mixed_rank": I.encoder_mixed_rank, "fused_layer": I.fused_layer}[args.workload]()
+    r.T = r.w.T
+    r.layers = 32
+    r.h = r.w.matrices[0].h_in
+    for _ in range(args.warmup):
+        r.cpu_sample(0.0)
+    vals, samples = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, s = r.cpu_sample(args.ref_step_seconds)
+        vals.append(v)
+        samples.append(s)
+    wall = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": samples[-1]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return str(dev)
+
+
+def run_ours(args, dist: Dist):
+    import torch
+    from segmented_gathered_rank_gb300 import lora as L
+    torch.cuda.set_device(dist.local_rank)
+    runner = RUNNERS[args.workload]()
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # Capture one step (and the dominant kernel's launches) as CUDA graphs.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(stream)          # warm the path once outside capture
+        torch.cuda.synchronize()
+        n0 = L.lora_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+        return g, L.lora_launch_count() - n0
+
+    g_step, launches_per_step = capture(runner.step)
+    g_dom, dom_launches = capture(runner.dominant_step)
+    torch.cuda.synchronize()
+    status = runner.pool.check_device_status()
+    if status:
+        raise RuntimeError(f"device status 0x{status:x} after the first step")
+
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(gpu_uuid(torch, dist.local_rank)) if dist.rank == 0 else None
+    if clocks:
+        clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop() if clocks else None
+    t_local = e0.elapsed_time(e1) / 1e3
+    value, t_max = aggregate(runner.units_per_step, args.steps, t_local, dist)
+    ms_per_step = 1e3 * t_max / args.steps
+
+    # Dominant kernel: its launches alone, replayed over the same number of steps.
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        d0.record(stream)
+        for _ in range(args.steps):
+            g_dom.replay()
+        d1.record(stream)
+    torch.cuda.synchronize()
+    dom = runner.dominant
+    per_launch_s = d0.elapsed_time(d1) / 1e3 / (args.steps * dom["launches_per_step"])
+    peaks, peak_src = load_peaks()
+    if dom["bound"] == "hbm":
+        achieved = dom["work_per_launch"] / per_launch_s / 1e9
+        peak = peaks["hbm_gbs"]
+    else:
+        achieved = dom["work_per_launch"] / per_launch_s / 1e12
+        peak = peaks["bf16_tflops"]
+    traffic_rec = load_traffic().get(args.workload)
+    traffic = None
+    if traffic_rec and traffic_rec.get("source_digest") == source_digest():
+        traffic = traffic_rec.get("dram_bytes_per_launch")
+
+    # End to end through the public API with host buffers.
+    runner.e2e_setup()
+    for _ in range(max(1, min(args.warmup, 3))):
+        runner.e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        runner.e2e_step()
+    torch.cuda.synchronize()
+    e2e_t = time.perf_counter() - t0
+    e2e_value, _ = aggregate(runner.units_per_step, args.steps, e2e_t, dist)
+    if runner.pool.check_device_status():
+        raise RuntimeError("device status set during the run")
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        v, sample = runner.cpu_sample(args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": sample}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
+            "config": {**runner.config, "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single"},
+            "roofline": {"bound": dom["bound"], "achieved": achieved, "peak": peak, "unit": dom["unit"],
+                         "frac": achieved / peak, "traffic": traffic, "kernel": dom["name"],
+                         "work_per_launch": dom["work_per_launch"], "launch_us": per_launch_s * 1e6,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(runner.h2d),
+                    "d2h_bytes_per_step": int(runner.d2h)},
+            "gpu_launches": int(launches_per_step * args.steps),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    runner.pool.close()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode_bgmv", choices=sorted(RUNNERS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--ref-step-seconds", type=float, default=1.0, help="reference-arm work per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, dist)
+        return run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

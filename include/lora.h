@@ -1,0 +1,202 @@
+/*
+ * lora.h -- C ABI of the GB300 multi-LoRA mixed-batch adapter library.
+ *
+ * The operation ("Multi-LoRA Serving - S-LoRA/Punica Batching, Adapter
+ * Hot-Swap & Memory", section "The kernel trick: gather, do not merge"): a
+ * request i that names adapter a(i) needs
+ *
+ *     y_i = x_i W^T + scale_a * (x_i A_a^T) B_a^T
+ *
+ * The base product is one matmul shared by the whole batch; the adapter term
+ * is a gather of small matmuls, "shrink" (x -> v, width r) then "expand"
+ * (v -> y).  SGMV serves contiguous segments of tokens that share an adapter
+ * (prefill), BGMV one adapter per token (decode).  Adapters of different
+ * ranks live in one paged pool ("A page holds H elements ... rank R -> R
+ * pages", S-LoRA slide 8) and are gathered without padding to a common rank
+ * (S-LoRA slide 10, MBGMM/MBGMV).
+ *
+ * Orientation used throughout.  For adapter a on one adapted matrix:
+ *   A_T_a is rank x h_in; its row j is the j-th low-rank direction, so
+ *         v[t][j] = sum_k x[t][k] * A_T_a[j][k];
+ *   B_a   is rank x h_out, and y[t][n] += scale_a * sum_j v[t][j] * B_a[j][n].
+ *   W     is h_out x h_in, row-major (row n = output feature n), like an
+ *         nn.Linear weight; the base term is y[t][n] = sum_k x[t][k] W[n][k].
+ *
+ * Conventions shared by every call:
+ *   - Element type: every x, y, W and page holds the pool's dtype (LORA_F32
+ *     or LORA_BF16).  v is always fp32.  Arithmetic accumulates in fp32;
+ *     bf16 results are rounded to nearest even on store.
+ *   - Layout: x is T x h_in, y is T x h_out, v is T x ld_v, all row-major and
+ *     dense (row stride = width).  Base pointers of x, y, v, W and the
+ *     workspace must be 16-byte aligned (torch allocations are).
+ *   - Pointers passed to compute calls are DEVICE pointers owned by the
+ *     caller; the library keeps none of them after the call returns.
+ *   - Streams: a lora_stream is a cudaStream_t (NULL = legacy default
+ *     stream).  Compute calls only enqueue work on it and never synchronise.
+ *   - Adapter ids: id < 0 means "no adapter" (the token keeps its base/y0
+ *     value).  An id >= max_adapters, or of an adapter not loaded on that
+ *     matrix, is a device-detected error: the token gets no adapter term and
+ *     bit LORA_DEV_BAD_ADAPTER is set in the pool's device status word.
+ *   - Segments: seg_starts has S+1 entries with seg_starts[0] == 0,
+ *     non-decreasing, seg_starts[S] == T; segment s covers tokens
+ *     seg_starts[s] .. seg_starts[s+1]-1 and uses adapter seg_adapter[s].
+ *     Empty segments are legal.  The table lives on the device, so it is
+ *     checked there: a violation sets LORA_DEV_BAD_SEGMENTS and the affected
+ *     tokens are computed against a clamped segment index (no access leaves
+ *     the arrays).
+ *   - Host-detectable errors (NULL pointer, bad size, misalignment, unknown
+ *     matrix, a pool of the wrong dtype) return a negative status before any
+ *     work is enqueued.  No kernel traps, asserts or waits without a bound.
+ *
+ * Thread safety: a pool may be used from one host thread at a time.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lora_pool lora_pool;   /* opaque; owns pages, tables, status word */
+typedef void *lora_stream;            /* a cudaStream_t */
+
+/* Return codes. */
+enum {
+    LORA_OK = 0,
+    LORA_ERR_ARG = -1,           /* bad argument (NULL, size, alignment, dtype) */
+    LORA_ERR_POOL_FULL = -2,     /* not enough free pages for the load */
+    LORA_ERR_RANK = -3,          /* rank < 0, rank > max_rank, or ld_v < max_rank */
+    LORA_ERR_NOT_LOADED = -4,    /* unload of an entry that holds no adapter */
+    LORA_ERR_CUDA = -5,          /* a CUDA runtime call failed (no device, OOM, ...) */
+    LORA_ERR_DEVICE_INDEX = -6,  /* lora_get_error: the device status word was non-zero */
+    LORA_ERR_SHAPE = -7          /* h_in/h_out disagree with the matrix or exceed the page */
+};
+
+/* Element types of the pool (and of x, y, W). */
+enum { LORA_F32 = 0, LORA_BF16 = 1 };
+
+/* Bits of the device status word (see lora_get_error). */
+enum {
+    LORA_DEV_BAD_ADAPTER = 1,    /* an id >= max_adapters, or an unloaded adapter */
+    LORA_DEV_BAD_SEGMENTS = 2,   /* a segment table that breaks the rules above */
+    LORA_DEV_WAIT_TIMEOUT = 4    /* a pipeline wait inside a kernel gave up */
+};
+
+/*
+ * Create a paged adapter pool on the current CUDA device.
+ *   dtype        LORA_F32 or LORA_BF16.
+ *   page_elems   H, elements per page; a multiple of 8 and >= every h_in and
+ *                h_out later loaded.  One page holds one row of A_T (h_in
+ *                elements) or one row of B (h_out elements).
+ *   n_pages      pages to allocate (device memory = n_pages*H*sizeof(dtype)).
+ *   max_rank     largest rank any adapter may have (1..1024).
+ *   n_matrices   number of adapted matrices (e.g. layers x projections).
+ *   max_adapters adapter ids run 0 .. max_adapters-1.
+ * A rank-r adapter on one matrix occupies exactly 2r pages (r for A_T, r for
+ * B), wherever they are free: ranks are mixed without padding (S-LoRA
+ * slides 8 and 10).  On success *out owns all device memory of the pool.
+ * Errors: LORA_ERR_ARG, LORA_ERR_CUDA (nothing is left allocated).
+ */
+int lora_pool_create(lora_pool **out, int dtype, int page_elems, int n_pages,
+                     int max_rank, int n_matrices, int max_adapters);
+
+/* Free every device and host resource of the pool.  Synchronises the device
+ * first.  NULL is accepted. */
+int lora_pool_destroy(lora_pool *pool);
+
+/*
+ * Load adapter `adapter` on matrix `matrix`: rank, scale, and HOST arrays
+ *   A_T  rank x h_in  (row-major, pool dtype),
+ *   B    rank x h_out (row-major, pool dtype).
+ * The first load on a matrix fixes that matrix's (h_in, h_out); later loads
+ * must match (else LORA_ERR_SHAPE).  A previous adapter in the same entry is
+ * replaced.  The host arrays are copied before the call returns (they may be
+ * freed at once); the device copy and the table update are enqueued on
+ * `stream`: work that uses the adapter must be ordered after them.
+ * rank == 0 is legal (the adapter adds nothing).
+ * Errors: LORA_ERR_ARG, LORA_ERR_RANK, LORA_ERR_SHAPE, LORA_ERR_POOL_FULL
+ * (the pool is unchanged), LORA_ERR_CUDA.
+ */
+int lora_pool_load(lora_pool *pool, int adapter, int matrix, int rank, float scale,
+                   int h_in, int h_out, const void *A_T, const void *B, lora_stream stream);
+
+/* Return the entry's pages to the free list and mark it unloaded.
+ * Synchronises the device first, so no queued kernel still reads the pages.
+ * Errors: LORA_ERR_ARG, LORA_ERR_NOT_LOADED, LORA_ERR_CUDA. */
+int lora_pool_unload(lora_pool *pool, int adapter, int matrix);
+
+/* Pages currently free (host bookkeeping; no device access). -1 on NULL. */
+int lora_pool_free_pages(const lora_pool *pool);
+
+/*
+ * SGMV shrink (prefill; MBGMM for mixed ranks):
+ *   v[t][j] = sum_k x[t][k] * A_T_a[j][k],  j < rank_a,  a = adapter of t's segment.
+ * x: T x h_in (pool dtype); v: T x ld_v fp32 with ld_v >= the pool's max_rank.
+ * Only v[t][0..rank_a-1] of tokens with a valid adapter are written.
+ * Errors: LORA_ERR_ARG, LORA_ERR_RANK (ld_v < max_rank), LORA_ERR_SHAPE.
+ */
+int lora_sgmv_shrink(lora_pool *pool, int matrix, const void *x, float *v, int ld_v,
+                     const int *seg_starts, const int *seg_adapter, int S, int T,
+                     lora_stream stream);
+
+/*
+ * SGMV expand:  y[t][n] += scale_a * sum_j v[t][j] * B_a[j][n]  (read-modify-write).
+ * v as produced by lora_sgmv_shrink; y: T x h_out (pool dtype).
+ * Errors as lora_sgmv_shrink.
+ */
+int lora_sgmv_expand(lora_pool *pool, int matrix, const float *v, int ld_v, void *y,
+                     const int *seg_starts, const int *seg_adapter, int S, int T,
+                     lora_stream stream);
+
+/*
+ * BGMV (decode; MBGMV for mixed ranks): shrink and expand fused, one adapter
+ * id per token:  y[t][n] += scale_a * sum_j (sum_k x[t][k] A_T_a[j][k]) B_a[j][n].
+ * x: T x h_in, y: T x h_out (read-modify-write), token_adapter: T device int32.
+ * Errors: LORA_ERR_ARG, LORA_ERR_SHAPE.
+ */
+int lora_bgmv(lora_pool *pool, int matrix, const void *x, void *y,
+              const int *token_adapter, int T, lora_stream stream);
+
+/* Bytes of device workspace lora_layer_forward needs for T tokens on this
+ * matrix (0 on a bad argument). */
+size_t lora_layer_forward_workspace_size(const lora_pool *pool, int matrix, int S, int T);
+
+/*
+ * Adapted layer: the shared base product for the whole mixed batch plus each
+ * token's own low-rank term ("runs the base matmul once, then applies each
+ * adapter's low-rank update"):
+ *   y[t][n] = sum_k x[t][k] * W[n][k] + scale_a * sum_j (sum_k x[t][k] A_T_a[j][k]) B_a[j][n]
+ * y is OVERWRITTEN.  W: h_out x h_in (pool dtype).  Tokens without an
+ * adapter (or with an invalid one) get the base term only.
+ * workspace: device scratch of at least lora_layer_forward_workspace_size()
+ * bytes, owned by the caller, contents undefined on entry and exit.
+ * Errors: LORA_ERR_ARG (includes ws_bytes too small), LORA_ERR_SHAPE.
+ */
+int lora_layer_forward(lora_pool *pool, int matrix, const void *x, const void *W, void *y,
+                       const int *seg_starts, const int *seg_adapter, int S, int T,
+                       void *workspace, size_t ws_bytes, lora_stream stream);
+
+/*
+ * Synchronise the device, read the pool's device status word into
+ * *device_status (may be NULL), and clear it.  Returns LORA_OK when the word
+ * was zero, LORA_ERR_DEVICE_INDEX when any LORA_DEV_* bit was set, or
+ * LORA_ERR_CUDA when the device reported an error.
+ */
+int lora_get_error(lora_pool *pool, int *device_status);
+
+/* Static English text for a return code. */
+const char *lora_strerror(int status);
+
+/* Kernels this library has launched since it was loaded (host-side count,
+ * summed over all pools; launches replayed from a captured CUDA graph are
+ * not counted again). */
+unsigned long long lora_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

@@ -1,0 +1,196 @@
+// Internal declarations shared by the library's translation units.
+//
+// Pool layout in HBM (all owned by lora_pool):
+//   pages   n_pages x page_elems elements of the pool dtype.  One page holds
+//           one row of A_T (h_in elements) or one row of B (h_out elements);
+//           a rank-r adapter on one matrix owns 2r pages anywhere in the
+//           pool ("A page holds H elements ... rank R -> R pages", S-LoRA
+//           slide 8), so mixed ranks need no padding.
+//   table   one record of rec_ints int32 per (adapter, matrix), record index
+//           adapter * n_matrices + matrix:
+//             [0] rank (-1 = not loaded)   [1] scale (float bits)
+//             [2] [3] reserved
+//             [4 .. 4+r)      page ids of the rows of A_T
+//             [4+r .. 4+2r)   page ids of the rows of B
+//           rec_ints = 4 + 2*max_rank rounded up to a multiple of 4, so a
+//           record starts on a 16-byte boundary.
+//   status  one int32 device status word (LORA_DEV_* bits).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <vector>
+
+#include "lora.h"
+
+namespace lora {
+
+constexpr int kRecHeader = 4;
+
+// Everything a kernel needs to resolve (adapter, matrix) -> rows of pages.
+struct PoolView {
+    void *pages;
+    const int *table;
+    int *status;
+    long long page_elems;
+    int rec_ints;
+    int n_matrices;
+    int max_adapters;
+    int max_rank;
+};
+
+extern std::atomic<unsigned long long> g_launches;
+inline void count_launch(int n = 1) { g_launches.fetch_add((unsigned long long)n); }
+
+}  // namespace lora
+
+struct lora_pool {
+    int device;
+    int dtype;
+    int esize;
+    int page_elems;
+    int n_pages;
+    int max_rank;
+    int n_matrices;
+    int max_adapters;
+    int rec_ints;
+    void *d_pages;
+    int *d_table;
+    int *d_status;
+    std::vector<int> free_pages;      // stack of free page ids
+    std::vector<int> host_table;      // mirror of the device table
+    std::vector<int> mat_h_in;        // per matrix, -1 until the first load
+    std::vector<int> mat_h_out;
+    // load staging: pinned host buffer -> device buffer -> scatter kernel
+    void *h_stage;
+    void *d_stage;
+    size_t stage_bytes;
+    cudaEvent_t stage_done;
+    bool stage_pending;
+
+    lora::PoolView view() const {
+        lora::PoolView v;
+        v.pages = d_pages;
+        v.table = d_table;
+        v.status = d_status;
+        v.page_elems = page_elems;
+        v.rec_ints = rec_ints;
+        v.n_matrices = n_matrices;
+        v.max_adapters = max_adapters;
+        v.max_rank = max_rank;
+        return v;
+    }
+};
+
+namespace lora {
+
+// ---------------------------------------------------------------------------
+// Host-side argument checks shared by the compute entry points.
+// ---------------------------------------------------------------------------
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Checks pool/matrix and returns LORA_OK with h_in/h_out filled in.
+inline int matrix_dims(const lora_pool *pool, int matrix, int *h_in, int *h_out) {
+    if (!pool || matrix < 0 || matrix >= pool->n_matrices) return LORA_ERR_ARG;
+    if (pool->mat_h_in[matrix] < 0) return LORA_ERR_SHAPE;   // nothing loaded on it yet
+    *h_in = pool->mat_h_in[matrix];
+    *h_out = pool->mat_h_out[matrix];
+    return LORA_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void flag(int *status, int bits) { atomicOr(status, bits); }
+
+// Record of (adapter a, matrix m), or nullptr after flagging an invalid id.
+__device__ __forceinline__ const int *lookup(const PoolView &pv, int a, int m) {
+    if (a >= pv.max_adapters) {
+        flag(pv.status, LORA_DEV_BAD_ADAPTER);
+        return nullptr;
+    }
+    const int *rec = pv.table + ((long long)a * pv.n_matrices + m) * pv.rec_ints;
+    if (rec[0] < 0) {
+        flag(pv.status, LORA_DEV_BAD_ADAPTER);
+        return nullptr;
+    }
+    return rec;
+}
+
+template <typename E>
+__device__ __forceinline__ const E *page_row(const PoolView &pv, int page) {
+    return reinterpret_cast<const E *>(pv.pages) + (long long)page * pv.page_elems;
+}
+
+// Segment containing token t: the last s in [0, S) with seg_starts[s] <= t
+// (so empty segments are skipped), clamped into range.
+__device__ __forceinline__ int segment_of(const int *seg_starts, int S, int t) {
+    int lo = 0, hi = S;   // first index in [0, S] whose start exceeds t
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(seg_starts + mid) > t) hi = mid; else lo = mid + 1;
+    }
+    int s = lo - 1;
+    return s < 0 ? 0 : (s >= S ? S - 1 : s);
+}
+
+// 8 consecutive elements <-> 8 floats (16-byte aligned for bf16; 32 for f32).
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float *o) {
+    uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(h[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const float *p, float *o) {
+    float4 a = *reinterpret_cast<const float4 *>(p);
+    float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float *o) {
+    uint4 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+    *reinterpret_cast<uint4 *>(p) = u;
+}
+__device__ __forceinline__ void store8(float *p, const float *o) {
+    *reinterpret_cast<float4 *>(p) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Checks a device segment table (one thread); sets LORA_DEV_BAD_SEGMENTS.
+__device__ __forceinline__ void check_segments(const int *seg_starts, int S, int T, int *status) {
+    bool bad = seg_starts[0] != 0 || seg_starts[S] != T;
+    for (int s = 0; s < S && !bad; ++s) bad = seg_starts[s + 1] < seg_starts[s];
+    if (bad) flag(status, LORA_DEV_BAD_SEGMENTS);
+}
+
+// ---------------------------------------------------------------------------
+// Launchers implemented in the kernel translation units.
+// ---------------------------------------------------------------------------
+int launch_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
+                  const int *seg_starts, const int *seg_adapter, int S, int T, cudaStream_t st);
+int launch_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
+                  const int *seg_starts, const int *seg_adapter, int S, int T, cudaStream_t st);
+int launch_bgmv(const lora_pool *pool, int matrix, int h_in, int h_out, const void *x, void *y,
+                const int *token_adapter, int T, cudaStream_t st);
+int launch_base_gemm(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y,
+                     int T, cudaStream_t st);
+
+}  // namespace lora

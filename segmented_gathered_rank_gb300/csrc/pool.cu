@@ -1,0 +1,319 @@
+// Paged adapter pool and the C-ABI entry points.
+//
+// The pool follows S-LoRA's unified paging ("A page holds H elements ...
+// rank R -> R pages", slide 8; "Adapters of different ranks ... would
+// fragment memory; one paged pool keeps utilisation high", "Multi-LoRA
+// Serving", question ladder L5): one device array of equal pages and a free
+// list, so adapters of any rank take exactly the pages they need.
+#include <cstring>
+#include <new>
+
+#include "internal.cuh"
+
+namespace lora {
+std::atomic<unsigned long long> g_launches{0};
+
+// Copies one staged row per block into its page and (block 0) writes the
+// record.  Staged layout: rows of A_T then rows of B, each `row_bytes[...]`
+// long, packed back to back at 16-byte multiples.
+struct LoadArgs {
+    int rec_index;
+    int rank;
+    float scale;
+    int row_bytes_a;
+    int row_bytes_b;
+    int ids[2 * 1024];
+};
+
+__global__ void load_scatter_kernel(const uint8_t *__restrict__ stage, uint8_t *__restrict__ pages,
+                                    long long page_bytes, int *__restrict__ table, int rec_ints,
+                                    const LoadArgs *__restrict__ args) {
+    const int row = blockIdx.x;
+    const int r = args->rank;
+    if (row < 2 * r) {
+        const bool is_a = row < r;
+        const int bytes = is_a ? args->row_bytes_a : args->row_bytes_b;
+        const long long src_off = is_a ? (long long)row * args->row_bytes_a
+                                       : (long long)r * args->row_bytes_a + (long long)(row - r) * args->row_bytes_b;
+        const uint4 *src = reinterpret_cast<const uint4 *>(stage + src_off);
+        uint4 *dst = reinterpret_cast<uint4 *>(pages + (long long)args->ids[row] * page_bytes);
+        for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) dst[i] = src[i];
+    }
+    if (row == 0) {
+        int *rec = table + (long long)args->rec_index * rec_ints;
+        for (int i = threadIdx.x; i < 2 * r; i += blockDim.x) rec[kRecHeader + i] = args->ids[i];
+        if (threadIdx.x == 0) {
+            rec[1] = __float_as_int(args->scale);
+            rec[2] = 0;
+            rec[3] = 0;
+            rec[0] = r;
+        }
+    }
+}
+
+__global__ void set_rank_kernel(int *table, long long rec_off, int rank) { table[rec_off] = rank; }
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+const char *lora_strerror(int status) {
+    switch (status) {
+        case LORA_OK: return "ok";
+        case LORA_ERR_ARG: return "invalid argument";
+        case LORA_ERR_POOL_FULL: return "adapter pool has too few free pages";
+        case LORA_ERR_RANK: return "rank out of range (or ld_v below the pool's max_rank)";
+        case LORA_ERR_NOT_LOADED: return "no adapter loaded in that entry";
+        case LORA_ERR_CUDA: return "CUDA runtime error";
+        case LORA_ERR_DEVICE_INDEX: return "device reported an invalid adapter id, segment table or wait timeout";
+        case LORA_ERR_SHAPE: return "h_in/h_out mismatch with the matrix, or larger than a page";
+        default: return "unknown status";
+    }
+}
+
+unsigned long long lora_launch_count(void) { return g_launches.load(); }
+
+int lora_pool_create(lora_pool **out, int dtype, int page_elems, int n_pages, int max_rank,
+                     int n_matrices, int max_adapters) {
+    if (!out) return LORA_ERR_ARG;
+    *out = nullptr;
+    if ((dtype != LORA_F32 && dtype != LORA_BF16) || page_elems <= 0 || page_elems % 8 != 0 ||
+        n_pages <= 0 || max_rank <= 0 || max_rank > 1024 || n_matrices <= 0 || max_adapters <= 0)
+        return LORA_ERR_ARG;
+    lora_pool *p = new (std::nothrow) lora_pool();
+    if (!p) return LORA_ERR_ARG;
+    p->dtype = dtype;
+    p->esize = dtype == LORA_F32 ? 4 : 2;
+    p->page_elems = page_elems;
+    p->n_pages = n_pages;
+    p->max_rank = max_rank;
+    p->n_matrices = n_matrices;
+    p->max_adapters = max_adapters;
+    p->rec_ints = (kRecHeader + 2 * max_rank + 3) & ~3;
+    p->d_pages = p->d_table = nullptr;
+    p->d_status = nullptr;
+    p->h_stage = p->d_stage = nullptr;
+    p->stage_done = nullptr;
+    p->stage_pending = false;
+    const size_t n_rec = (size_t)max_adapters * n_matrices;
+    p->stage_bytes = (size_t)2 * max_rank * page_elems * p->esize + 256 + sizeof(LoadArgs);
+    int rc = LORA_OK;
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaMalloc(&p->d_pages, (size_t)n_pages * page_elems * p->esize) != cudaSuccess ||
+        cudaMalloc((void **)&p->d_table, n_rec * p->rec_ints * sizeof(int)) != cudaSuccess ||
+        cudaMalloc((void **)&p->d_status, sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&p->d_stage, p->stage_bytes) != cudaSuccess ||
+        cudaMallocHost(&p->h_stage, p->stage_bytes) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->stage_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaMemset(p->d_table, 0xFF, n_rec * p->rec_ints * sizeof(int)) != cudaSuccess ||   // rank -1
+        cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        rc = LORA_ERR_CUDA;
+    if (rc != LORA_OK) {
+        cudaGetLastError();
+        lora_pool_destroy(p);
+        return rc;
+    }
+    try {
+        p->free_pages.resize(n_pages);
+        for (int i = 0; i < n_pages; ++i) p->free_pages[i] = n_pages - 1 - i;   // pop gives 0,1,2...
+        p->host_table.assign(n_rec * p->rec_ints, -1);
+        p->mat_h_in.assign(n_matrices, -1);
+        p->mat_h_out.assign(n_matrices, -1);
+    } catch (...) {
+        lora_pool_destroy(p);
+        return LORA_ERR_ARG;
+    }
+    *out = p;
+    return LORA_OK;
+}
+
+int lora_pool_destroy(lora_pool *p) {
+    if (!p) return LORA_OK;
+    cudaDeviceSynchronize();
+    if (p->d_pages) cudaFree(p->d_pages);
+    if (p->d_table) cudaFree(p->d_table);
+    if (p->d_status) cudaFree(p->d_status);
+    if (p->d_stage) cudaFree(p->d_stage);
+    if (p->h_stage) cudaFreeHost(p->h_stage);
+    if (p->stage_done) cudaEventDestroy(p->stage_done);
+    cudaGetLastError();
+    delete p;
+    return LORA_OK;
+}
+
+int lora_pool_free_pages(const lora_pool *p) { return p ? (int)p->free_pages.size() : -1; }
+
+// Frees the pages of record `ri` on the host side (device untouched).
+static void release_pages(lora_pool *p, size_t ri) {
+    int *rec = &p->host_table[ri * p->rec_ints];
+    int r = rec[0];
+    for (int i = 0; i < 2 * r; ++i) p->free_pages.push_back(rec[kRecHeader + i]);
+    rec[0] = -1;
+}
+
+int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale, int h_in, int h_out,
+                   const void *A_T, const void *B, lora_stream stream) {
+    if (!p || adapter < 0 || adapter >= p->max_adapters || matrix < 0 || matrix >= p->n_matrices)
+        return LORA_ERR_ARG;
+    if (rank < 0 || rank > p->max_rank) return LORA_ERR_RANK;
+    if (h_in <= 0 || h_out <= 0 || h_in % 8 || h_out % 8) return LORA_ERR_ARG;
+    if (h_in > p->page_elems || h_out > p->page_elems) return LORA_ERR_SHAPE;
+    if (p->mat_h_in[matrix] >= 0 && (p->mat_h_in[matrix] != h_in || p->mat_h_out[matrix] != h_out))
+        return LORA_ERR_SHAPE;
+    if (rank > 0 && (!A_T || !B)) return LORA_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t ri = (size_t)adapter * p->n_matrices + matrix;
+    int *hrec = &p->host_table[ri * p->rec_ints];
+    const int old_rank = hrec[0];
+    if ((int)p->free_pages.size() + (old_rank > 0 ? 2 * old_rank : 0) < 2 * rank) return LORA_ERR_POOL_FULL;
+    if (old_rank >= 0) {
+        // Replacing: queued kernels may still read the old pages.
+        if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
+        release_pages(p, ri);
+    }
+    // The staging buffers are reused: wait for the previous load's scatter.
+    if (p->stage_pending) {
+        if (cudaEventSynchronize(p->stage_done) != cudaSuccess) return LORA_ERR_CUDA;
+        p->stage_pending = false;
+    }
+    const int rba = h_in * p->esize, rbb = h_out * p->esize;
+    const size_t data_bytes = (size_t)rank * (rba + rbb);
+    const size_t args_off = (data_bytes + 255) & ~(size_t)255;
+    uint8_t *hs = (uint8_t *)p->h_stage;
+    if (rank > 0) {
+        std::memcpy(hs, A_T, (size_t)rank * rba);
+        std::memcpy(hs + (size_t)rank * rba, B, (size_t)rank * rbb);
+    }
+    LoadArgs *la = reinterpret_cast<LoadArgs *>(hs + args_off);
+    la->rec_index = (int)ri;
+    la->rank = rank;
+    la->scale = scale;
+    la->row_bytes_a = rba;
+    la->row_bytes_b = rbb;
+    for (int i = 0; i < 2 * rank; ++i) {
+        la->ids[i] = p->free_pages.back();
+        p->free_pages.pop_back();
+    }
+    const size_t copy_bytes = args_off + offsetof(LoadArgs, ids) + sizeof(int) * 2 * rank;
+    cudaError_t e = cudaMemcpyAsync(p->d_stage, p->h_stage, copy_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) {
+        const uint8_t *ds = (const uint8_t *)p->d_stage;
+        load_scatter_kernel<<<rank > 0 ? 2 * rank : 1, 256, 0, st>>>(
+            ds, (uint8_t *)p->d_pages, (long long)p->page_elems * p->esize, p->d_table, p->rec_ints,
+            reinterpret_cast<const LoadArgs *>(ds + args_off));
+        count_launch();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(p->stage_done, st);
+    if (e != cudaSuccess) {
+        for (int i = 2 * rank - 1; i >= 0; --i) p->free_pages.push_back(la->ids[i]);
+        return LORA_ERR_CUDA;
+    }
+    p->stage_pending = true;
+    hrec[0] = rank;
+    std::memcpy(&hrec[1], &scale, sizeof(int));
+    for (int i = 0; i < 2 * rank; ++i) hrec[kRecHeader + i] = la->ids[i];
+    p->mat_h_in[matrix] = h_in;
+    p->mat_h_out[matrix] = h_out;
+    return LORA_OK;
+}
+
+int lora_pool_unload(lora_pool *p, int adapter, int matrix) {
+    if (!p || adapter < 0 || adapter >= p->max_adapters || matrix < 0 || matrix >= p->n_matrices)
+        return LORA_ERR_ARG;
+    const size_t ri = (size_t)adapter * p->n_matrices + matrix;
+    if (p->host_table[ri * p->rec_ints] < 0) return LORA_ERR_NOT_LOADED;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
+    set_rank_kernel<<<1, 1>>>(p->d_table, (long long)ri * p->rec_ints, -1);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
+    release_pages(p, ri);
+    return LORA_OK;
+}
+
+int lora_get_error(lora_pool *p, int *device_status) {
+    if (device_status) *device_status = 0;
+    if (!p) return LORA_ERR_ARG;
+    int word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    if (device_status) *device_status = word;
+    return word ? LORA_ERR_DEVICE_INDEX : LORA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Compute entry points: argument checks, then the launchers.
+// ---------------------------------------------------------------------------
+static int check_common(const lora_pool *p, int S, int T) {
+    if (!p || T < 0 || S < 0) return LORA_ERR_ARG;
+    if (S == 0 && T > 0) return LORA_ERR_ARG;
+    return LORA_OK;
+}
+
+int lora_sgmv_shrink(lora_pool *p, int matrix, const void *x, float *v, int ld_v, const int *seg_starts,
+                     const int *seg_adapter, int S, int T, lora_stream stream) {
+    int rc = check_common(p, S, T);
+    if (rc) return rc;
+    int h_in, h_out;
+    if ((rc = matrix_dims(p, matrix, &h_in, &h_out))) return rc;
+    if (ld_v < p->max_rank) return LORA_ERR_RANK;
+    if (T == 0) return LORA_OK;
+    if (!x || !v || !seg_starts || !seg_adapter || !aligned16(x) || !aligned16(v)) return LORA_ERR_ARG;
+    return launch_shrink(p, matrix, h_in, x, v, ld_v, seg_starts, seg_adapter, S, T, (cudaStream_t)stream);
+}
+
+int lora_sgmv_expand(lora_pool *p, int matrix, const float *v, int ld_v, void *y, const int *seg_starts,
+                     const int *seg_adapter, int S, int T, lora_stream stream) {
+    int rc = check_common(p, S, T);
+    if (rc) return rc;
+    int h_in, h_out;
+    if ((rc = matrix_dims(p, matrix, &h_in, &h_out))) return rc;
+    if (ld_v < p->max_rank) return LORA_ERR_RANK;
+    if (T == 0) return LORA_OK;
+    if (!y || !v || !seg_starts || !seg_adapter || !aligned16(y) || !aligned16(v)) return LORA_ERR_ARG;
+    return launch_expand(p, matrix, h_out, v, ld_v, y, seg_starts, seg_adapter, S, T, (cudaStream_t)stream);
+}
+
+int lora_bgmv(lora_pool *p, int matrix, const void *x, void *y, const int *token_adapter, int T,
+              lora_stream stream) {
+    if (!p || T < 0) return LORA_ERR_ARG;
+    int h_in, h_out, rc;
+    if ((rc = matrix_dims(p, matrix, &h_in, &h_out))) return rc;
+    if (T == 0) return LORA_OK;
+    if (!x || !y || !token_adapter || !aligned16(x) || !aligned16(y)) return LORA_ERR_ARG;
+    return launch_bgmv(p, matrix, h_in, h_out, x, y, token_adapter, T, (cudaStream_t)stream);
+}
+
+size_t lora_layer_forward_workspace_size(const lora_pool *p, int matrix, int S, int T) {
+    int h_in, h_out;
+    if (!p || T < 0 || S < 0 || matrix_dims(p, matrix, &h_in, &h_out)) return 0;
+    return (size_t)T * p->max_rank * sizeof(float) + 256;
+}
+
+int lora_layer_forward(lora_pool *p, int matrix, const void *x, const void *W, void *y,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, void *workspace,
+                       size_t ws_bytes, lora_stream stream) {
+    int rc = check_common(p, S, T);
+    if (rc) return rc;
+    int h_in, h_out;
+    if ((rc = matrix_dims(p, matrix, &h_in, &h_out))) return rc;
+    if (T == 0) return LORA_OK;
+    if (!x || !W || !y || !seg_starts || !seg_adapter || !workspace || !aligned16(x) || !aligned16(W) ||
+        !aligned16(y) || !aligned16(workspace))
+        return LORA_ERR_ARG;
+    if (ws_bytes < lora_layer_forward_workspace_size(p, matrix, S, T)) return LORA_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    float *v = (float *)workspace;
+    if ((rc = launch_base_gemm(p, h_in, h_out, x, W, y, T, st))) return rc;
+    if ((rc = launch_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, st))) return rc;
+    return launch_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+"""Thin ctypes binding of ``include/lora.h`` (argument marshalling only).
+
+Every function has the name of the C entry point it calls.  Device arguments
+are CUDA torch tensors (their data pointers are passed), host arrays for
+``lora_pool_load`` are numpy arrays or CPU tensors, and ``stream`` defaults to
+torch's current stream.  A non-zero status raises :class:`LoraError`.  All
+arithmetic happens in the CUDA library; importing this module fails when the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+LORA_OK = 0
+LORA_ERR_ARG = -1
+LORA_ERR_POOL_FULL = -2
+LORA_ERR_RANK = -3
+LORA_ERR_NOT_LOADED = -4
+LORA_ERR_CUDA = -5
+LORA_ERR_DEVICE_INDEX = -6
+LORA_ERR_SHAPE = -7
+
+LORA_F32 = 0
+LORA_BF16 = 1
+
+LORA_DEV_BAD_ADAPTER = 1
+LORA_DEV_BAD_SEGMENTS = 2
+LORA_DEV_WAIT_TIMEOUT = 4
+
+EXPORTS = ["lora_pool_create", "lora_pool_destroy", "lora_pool_load", "lora_pool_unload",
+           "lora_pool_free_pages", "lora_sgmv_shrink", "lora_sgmv_expand", "lora_bgmv",
+           "lora_layer_forward_workspace_size", "lora_layer_forward", "lora_get_error", "lora_strerror",
+           "lora_launch_count"]
+
+if not os.path.exists(_build.LIB):
+    raise ImportError(f"CUDA library {_build.LIB} is not built: run segmented_gathered_rank_gb300.build.build()")
+
+LIB_PATH = _build.LIB
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("lora_pool_create", _I, ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I)
+_sig("lora_pool_destroy", _I, _P)
+_sig("lora_pool_load", _I, _P, _I, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P)
+_sig("lora_pool_unload", _I, _P, _I, _I)
+_sig("lora_pool_free_pages", _I, _P)
+_sig("lora_sgmv_shrink", _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _P)
+_sig("lora_sgmv_expand", _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _P)
+_sig("lora_bgmv", _I, _P, _I, _P, _P, _P, _I, _P)
+_sig("lora_layer_forward_workspace_size", ctypes.c_size_t, _P, _I, _I, _I)
+_sig("lora_layer_forward", _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P, ctypes.c_size_t, _P)
+_sig("lora_get_error", _I, _P, ctypes.POINTER(_I))
+_sig("lora_strerror", ctypes.c_char_p, _I)
+_sig("lora_launch_count", ctypes.c_ulonglong)
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str, device_status: int = 0):
+        self.status = status
+        self.device_status = device_status
+        msg = f"{where}: {lora_strerror(status)} ({status})"
+        if device_status:
+            msg += f", device status 0x{device_status:x}"
+        super().__init__(msg)
+
+
+def _check(rc: int, where: str):
+    if rc != LORA_OK:
+        raise LoraError(rc, where)
+
+
+def _dptr(t):
+    """Device pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hptr(a):
+    """Host pointer of a numpy array or CPU tensor (kept alive by the caller)."""
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        if not a.flags.c_contiguous:
+            raise ValueError("expected a C-contiguous host array")
+        return ctypes.c_void_p(a.ctypes.data)
+    if a.is_cuda or not a.is_contiguous():
+        raise ValueError("expected a contiguous CPU tensor")
+    return ctypes.c_void_p(a.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def lora_strerror(status: int) -> str:
+    return _lib.lora_strerror(int(status)).decode()
+
+
+def lora_launch_count() -> int:
+    return int(_lib.lora_launch_count())
+
+
+def lora_pool_create(dtype: int, page_elems: int, n_pages: int, max_rank: int, n_matrices: int,
+                     max_adapters: int) -> int:
+    """Returns the pool handle (an opaque address)."""
+    h = ctypes.c_void_p()
+    _check(_lib.lora_pool_create(ctypes.byref(h), dtype, page_elems, n_pages, max_rank, n_matrices,
+                                 max_adapters), "lora_pool_create")
+    return h.value
+
+
+def lora_pool_destroy(pool) -> None:
+    _check(_lib.lora_pool_destroy(pool), "lora_pool_destroy")
+
+
+def lora_pool_load(pool, adapter: int, matrix: int, rank: int, scale: float, h_in: int, h_out: int,
+                   A_T, B, stream=None) -> None:
+    _check(_lib.lora_pool_load(pool, adapter, matrix, rank, float(scale), h_in, h_out, _hptr(A_T), _hptr(B),
+                               _stream(stream)), "lora_pool_load")
+
+
+def lora_pool_unload(pool, adapter: int, matrix: int) -> None:
+    _check(_lib.lora_pool_unload(pool, adapter, matrix), "lora_pool_unload")
+
+
+def lora_pool_free_pages(pool) -> int:
+    return int(_lib.lora_pool_free_pages(pool))
+
+
+def lora_sgmv_shrink(pool, matrix, x, v, ld_v, seg_starts, seg_adapter, S, T, stream=None) -> None:
+    _check(_lib.lora_sgmv_shrink(pool, matrix, _dptr(x), _dptr(v), ld_v, _dptr(seg_starts), _dptr(seg_adapter),
+                                 S, T, _stream(stream)), "lora_sgmv_shrink")
+
+
+def lora_sgmv_expand(pool, matrix, v, ld_v, y, seg_starts, seg_adapter, S, T, stream=None) -> None:
+    _check(_lib.lora_sgmv_expand(pool, matrix, _dptr(v), ld_v, _dptr(y), _dptr(seg_starts), _dptr(seg_adapter),
+                                 S, T, _stream(stream)), "lora_sgmv_expand")
+
+
+def lora_bgmv(pool, matrix, x, y, token_adapter, T, stream=None) -> None:
+    _check(_lib.lora_bgmv(pool, matrix, _dptr(x), _dptr(y), _dptr(token_adapter), T, _stream(stream)),
+           "lora_bgmv")
+
+
+def lora_layer_forward_workspace_size(pool, matrix, S, T) -> int:
+    return int(_lib.lora_layer_forward_workspace_size(pool, matrix, S, T))
+
+
+def lora_layer_forward(pool, matrix, x, W, y, seg_starts, seg_adapter, S, T, workspace, ws_bytes=None,
+                       stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.lora_layer_forward(pool, matrix, _dptr(x), _dptr(W), _dptr(y), _dptr(seg_starts),
+                                   _dptr(seg_adapter), S, T, _dptr(workspace), ws_bytes, _stream(stream)),
+           "lora_layer_forward")
+
+
+def lora_get_error(pool) -> tuple[int, int]:
+    """(status, device status word); the word is cleared."""
+    word = ctypes.c_int(0)
+    rc = _lib.lora_get_error(pool, ctypes.byref(word))
+    return int(rc), int(word.value)

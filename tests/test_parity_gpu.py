@@ -1,0 +1,361 @@
+"""GPU parity: every entry point against the CPU oracle on seeded inputs.
+
+Covers the five workloads at full size (the fused layer on sampled rows),
+small randomized ragged cases, integer probes compared bit for bit, and the
+edge cases (empty segments, tokens without an adapter, invalid ids, bad
+segment tables, rank 0, T = 0, pool exhaustion and page reuse).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import oracle  # noqa: E402
+from segmented_gathered_rank_gb300 import harness as H  # noqa: E402
+from segmented_gathered_rank_gb300 import inputs as I  # noqa: E402
+from segmented_gathered_rank_gb300 import lora as L  # noqa: E402
+from tests.parity import (TOL_V, TOL_Y, oracle_delta, oracle_v, rel_err, sample_rows,  # noqa: E402
+                          written_mask)
+
+
+def _tables(w):
+    return H.int_tensor(w.seg_starts), H.int_tensor(w.seg_adapter)
+
+
+def run_sgmv(w, m=0, zero_y0=False):
+    """shrink then expand on one matrix; returns (v, y, device status)."""
+    with H.DevicePool(w, matrices=[m]) as dp:
+        ss, sa = _tables(w)
+        x = H.to_device(w.x(m), w.dtype)
+        y0 = np.zeros((w.T, w.matrices[m].h_out), np.float32) if zero_y0 else w.y0(m)
+        y = H.to_device(y0, w.dtype)
+        ld_v = w.max_rank
+        v = torch.full((w.T, ld_v), float("nan"), dtype=torch.float32, device="cuda")
+        L.lora_sgmv_shrink(dp.handle, 0, x, v, ld_v, ss, sa, w.S, w.T)
+        L.lora_sgmv_expand(dp.handle, 0, v, ld_v, y, ss, sa, w.S, w.T)
+        word = dp.check_device_status()
+        return H.to_host(v), H.to_host(y), y0, word
+
+
+def run_bgmv(w, m=0, zero_y0=False):
+    with H.DevicePool(w, matrices=[m]) as dp:
+        ids = w.token_adapter if w.token_adapter is not None else w.seg_adapter
+        tok = H.int_tensor(ids)
+        x = H.to_device(w.x(m), w.dtype)
+        y0 = np.zeros((w.T, w.matrices[m].h_out), np.float32) if zero_y0 else w.y0(m)
+        y = H.to_device(y0, w.dtype)
+        L.lora_bgmv(dp.handle, 0, x, y, tok, w.T)
+        word = dp.check_device_status()
+        return H.to_host(y), y0, word
+
+
+def run_layer(w, m=0, zero_w=False):
+    with H.DevicePool(w, matrices=[m]) as dp:
+        ss, sa = _tables(w)
+        x = H.to_device(w.x(m), w.dtype)
+        Wh = np.zeros((w.matrices[m].h_out, w.matrices[m].h_in), np.float32) if zero_w else w.W(m)
+        Wd = H.to_device(Wh, w.dtype)
+        y = torch.full((w.T, w.matrices[m].h_out), float("nan"), dtype=H.torch_dtype(w.dtype), device="cuda")
+        ws_bytes = L.lora_layer_forward_workspace_size(dp.handle, 0, w.S, w.T)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        L.lora_layer_forward(dp.handle, 0, x, Wd, y, ss, sa, w.S, w.T, ws)
+        word = dp.check_device_status()
+        return H.to_host(y), Wh, word
+
+
+def check_sgmv(w, m=0, rows=None):
+    for zero in (True, False):
+        v, y, y0, word = run_sgmv(w, m, zero_y0=zero)
+        assert word == 0
+        vr, st = oracle_v(w, m, w.max_rank)
+        assert st == 0
+        mask = written_mask(w, w.max_rank)
+        assert not np.isnan(v[mask]).any()
+        assert rel_err(v[mask], vr[mask]) <= TOL_V[w.dtype]
+        yr, st = oracle_delta(w, m, y0)
+        assert st == 0
+        e = rel_err(y, yr)
+        assert e <= TOL_Y[w.dtype], (zero, e)
+
+
+def check_bgmv(w, m=0):
+    for zero in (True, False):
+        y, y0, word = run_bgmv(w, m, zero_y0=zero)
+        assert word == 0
+        yr, st = oracle_delta(w, m, y0)
+        assert st == 0
+        e = rel_err(y, yr)
+        assert e <= TOL_Y[w.dtype], (zero, e)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads
+# ---------------------------------------------------------------------------
+def test_tiny_sgmv_f32():
+    check_sgmv(I.tiny_sgmv())
+
+
+def test_tiny_layer_f32():
+    w = I.tiny_sgmv()
+    y, Wh, word = run_layer(w)
+    assert word == 0
+    yr, st = oracle_delta(w, 0, None, W=Wh)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+
+
+def test_decode_bgmv_full():
+    check_bgmv(I.decode_bgmv())
+
+
+def test_decode_batch_as_unit_segments():
+    check_sgmv(I.decode_bgmv())
+
+
+@pytest.mark.parametrize("m", [0, 1])   # q (4096 -> 4096) and k (4096 -> 1024)
+def test_prefill_sgmv_full(m):
+    check_sgmv(I.prefill_sgmv(), m)
+
+
+@pytest.mark.parametrize("m", [0, 47])
+def test_encoder_mixed_rank_full(m):
+    check_sgmv(I.encoder_mixed_rank(), m)
+
+
+def test_encoder_mixed_rank_bgmv():
+    """The same mixed-rank batch through BGMV, one adapter id per token (MBGMV)."""
+    w = I.encoder_mixed_rank()
+    w.token_adapter = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+    check_bgmv(w, 5)
+
+
+def _fused_rows(w):
+    rng = np.random.default_rng(1)
+    rows = set()
+    for s in range(4):
+        lo, hi = int(w.seg_starts[s]), int(w.seg_starts[s + 1])
+        rows.update({lo, lo + 1, lo + 127, lo + 128, hi - 1})
+    rows.update(rng.integers(0, 4096, 24).tolist())
+    dec = np.arange(4096, 4608)
+    rows.update(rng.choice(dec, 40, replace=False).tolist())
+    rows.update(dec[w.seg_adapter[4:] == 0][:8].tolist())   # the rank-128 adapter at decode
+    rows.add(4607)
+    return np.array(sorted(rows), np.int32)
+
+
+@pytest.mark.parametrize("m", [0, 1, 3])
+def test_fused_layer_sampled(m):
+    w = I.fused_layer()
+    rows = _fused_rows(w)
+    y, Wh, word = run_layer(w, m)
+    assert word == 0
+    yr, st = oracle_delta(w, m, None, rows=rows, W=Wh)
+    assert st == 0
+    assert rel_err(y[rows], yr) <= TOL_Y[w.dtype]
+
+
+def test_fused_layer_delta_alone():
+    w = I.fused_layer()
+    rows = _fused_rows(w)
+    y, Wh, word = run_layer(w, 0, zero_w=True)
+    assert word == 0
+    yr, st = oracle_delta(w, 0, None, rows=rows)
+    assert st == 0
+    assert rel_err(y[rows], yr) <= TOL_Y[w.dtype]
+
+
+# ---------------------------------------------------------------------------
+# Small randomized cases: ragged segments (some empty), ragged ranks,
+# tokens without an adapter, T off the tile grid.
+# ---------------------------------------------------------------------------
+RANDOM = [
+    dict(seed=1, T=1, lengths=[1]),
+    dict(seed=2, T=77, lengths=[0, 30, 0, 47, 0]),
+    dict(seed=3, T=300, none_fraction=0.3),
+    dict(seed=4, T=257, h_in=72, h_out=40),
+    dict(seed=5, T=513, h_in=1024, h_out=520, ranks=[8, 64, 16, 32, 1]),
+    dict(seed=6, T=129, dtype=I.F32, h_in=96, h_out=128),
+    dict(seed=7, T=1000, h_in=4096, h_out=1024, ranks=[16, 128, 16, 4]),
+]
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=lambda c: f"seed{c['seed']}")
+def test_random_sgmv(case):
+    check_sgmv(I.random_case(**case))
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=lambda c: f"seed{c['seed']}")
+def test_random_bgmv(case):
+    c = dict(case)
+    c.pop("lengths", None)
+    check_bgmv(I.random_case(decode=True, **c))
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=lambda c: f"seed{c['seed']}")
+def test_random_layer(case):
+    w = I.random_case(**case)
+    y, Wh, word = run_layer(w)
+    assert word == 0
+    yr, st = oracle_delta(w, 0, None, W=Wh)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+
+
+# ---------------------------------------------------------------------------
+# Integer probes: every partial sum exact -> bit-exact agreement.
+# ---------------------------------------------------------------------------
+PROBES = [
+    dict(seed=11, T=40, lengths=[10, 0, 30], h_in=64, h_out=48, ranks=[4, 8]),
+    dict(seed=12, T=300, lengths=[128, 1, 0, 171], h_in=512, h_out=256, ranks=[16, 2, 32], none_fraction=0.2),
+    dict(seed=13, T=260, lengths=[130, 130], h_in=4096, h_out=1024, ranks=[16, 128]),
+]
+
+
+def _exact(a):
+    return np.array_equal(np.asarray(a, np.float64), np.round(np.asarray(a, np.float64)))
+
+
+@pytest.mark.parametrize("dtype", [I.BF16, I.F32])
+@pytest.mark.parametrize("case", PROBES, ids=lambda c: f"seed{c['seed']}")
+def test_integer_probe_bitexact(case, dtype):
+    w = I.integer_probe(dtype=dtype, **case)
+    v, y, y0, word = run_sgmv(w)
+    assert word == 0
+    vr, _ = oracle_v(w, 0, w.max_rank)
+    mask = written_mask(w, w.max_rank)
+    assert _exact(vr[mask]) and np.array_equal(v[mask], vr[mask])
+    yr, _ = oracle_delta(w, 0, y0)
+    assert _exact(yr) and np.max(np.abs(yr)) <= 256
+    assert np.array_equal(y, yr)
+    yl, Wh, word = run_layer(w)
+    assert word == 0
+    ylr, _ = oracle_delta(w, 0, None, W=Wh)
+    assert _exact(ylr) and np.max(np.abs(ylr)) <= 256
+    assert np.array_equal(yl, ylr)
+    wd = I.integer_probe(dtype=dtype, **case)
+    wd.token_adapter = np.repeat(wd.seg_adapter, np.diff(wd.seg_starts)).astype(np.int32)
+    yb, y0b, word = run_bgmv(wd)
+    assert word == 0
+    assert np.array_equal(yb, yr)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases and faults (host-made; nothing traps)
+# ---------------------------------------------------------------------------
+def test_invalid_ids_are_flagged_and_skipped():
+    w = I.random_case(21, T=64, lengths=[16, 16, 16, 16], n_adapters=3, ranks=[4, 8, 4])
+    w.seg_adapter = np.array([0, 5, 1, 2], np.int32)       # 5 >= max_adapters
+    with H.DevicePool(w, load_ids=[0, 1]) as dp:             # 2 is not loaded
+        ss, sa = _tables(w)
+        x = H.to_device(w.x(), w.dtype)
+        y0 = w.y0()
+        y = H.to_device(y0, w.dtype)
+        v = torch.zeros((w.T, w.max_rank), dtype=torch.float32, device="cuda")
+        L.lora_sgmv_shrink(dp.handle, 0, x, v, w.max_rank, ss, sa, w.S, w.T)
+        L.lora_sgmv_expand(dp.handle, 0, v, w.max_rank, y, ss, sa, w.S, w.T)
+        rc, word = L.lora_get_error(dp.handle)
+        assert rc == L.LORA_ERR_DEVICE_INDEX and word == L.LORA_DEV_BAD_ADAPTER
+        assert L.lora_get_error(dp.handle) == (L.LORA_OK, 0)     # cleared
+        yh = H.to_host(y)
+        assert np.array_equal(yh[16:32], y0[16:32]) and np.array_equal(yh[48:64], y0[48:64])
+        yr, st = oracle_delta(w, 0, y0, ids=[0, 1])
+        assert st == oracle.ERR_ADAPTER
+        assert rel_err(yh, yr) <= TOL_Y[w.dtype]
+
+
+def test_bad_segment_table_is_flagged():
+    w = I.random_case(22, T=32, lengths=[16, 16], n_adapters=2, ranks=[4, 4])
+    with H.DevicePool(w) as dp:
+        x = H.to_device(w.x(), w.dtype)
+        v = torch.zeros((w.T, w.max_rank), dtype=torch.float32, device="cuda")
+        for bad in ([0, 20, 16], [1, 16, 32], [0, 16, 31]):
+            ss = H.int_tensor(bad)
+            sa = H.int_tensor(w.seg_adapter)
+            L.lora_sgmv_shrink(dp.handle, 0, x, v, w.max_rank, ss, sa, 2, 32)
+            rc, word = L.lora_get_error(dp.handle)
+            assert rc == L.LORA_ERR_DEVICE_INDEX and word & L.LORA_DEV_BAD_SEGMENTS
+
+
+def test_zero_tokens_and_host_errors():
+    w = I.random_case(23, T=16, lengths=[16], n_adapters=1, ranks=[4])
+    with H.DevicePool(w) as dp:
+        x = H.to_device(w.x(), w.dtype)
+        y = H.to_device(w.y0(), w.dtype)
+        v = torch.zeros((16, w.max_rank), dtype=torch.float32, device="cuda")
+        ss, sa = _tables(w)
+        n0 = L.lora_launch_count()
+        L.lora_sgmv_shrink(dp.handle, 0, x, v, w.max_rank, ss, sa, 1, 0)
+        L.lora_bgmv(dp.handle, 0, x, y, sa, 0)
+        assert L.lora_launch_count() == n0
+        with pytest.raises(L.LoraError) as e:
+            L.lora_sgmv_shrink(dp.handle, 0, x, v, w.max_rank - 1, ss, sa, 1, 16)
+        assert e.value.status == L.LORA_ERR_RANK
+        with pytest.raises(L.LoraError) as e:
+            L.lora_sgmv_shrink(dp.handle, 3, x, v, w.max_rank, ss, sa, 1, 16)
+        assert e.value.status == L.LORA_ERR_ARG
+        with pytest.raises(L.LoraError) as e:
+            L.lora_bgmv(dp.handle, 0, None, y, sa, 16)
+        assert e.value.status == L.LORA_ERR_ARG
+
+
+def test_pool_lifecycle():
+    h_in = h_out = 256
+    pool = L.lora_pool_create(L.LORA_BF16, 256, 40, 16, 2, 4)
+    try:
+        rng = np.random.default_rng(0)
+
+        def arr(r, h):
+            return I.bf16_bits(I.round_to_bf16(rng.normal(size=(r, h)).astype(np.float32)))
+
+        assert L.lora_pool_free_pages(pool) == 40
+        L.lora_pool_load(pool, 0, 0, 8, 1.0, h_in, h_out, arr(8, h_in), arr(8, h_out))
+        assert L.lora_pool_free_pages(pool) == 24
+        L.lora_pool_load(pool, 1, 1, 0, 1.0, h_in, h_out, None, None)            # rank 0
+        assert L.lora_pool_free_pages(pool) == 24
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pool_load(pool, 2, 0, 16, 1.0, h_in, h_out, arr(16, h_in), arr(16, h_out))
+        assert e.value.status == L.LORA_ERR_POOL_FULL
+        assert L.lora_pool_free_pages(pool) == 24
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pool_load(pool, 2, 0, 17, 1.0, h_in, h_out, arr(17, h_in), arr(17, h_out))
+        assert e.value.status == L.LORA_ERR_RANK
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pool_load(pool, 2, 0, 4, 1.0, 128, h_out, arr(4, 128), arr(4, h_out))
+        assert e.value.status == L.LORA_ERR_SHAPE
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pool_unload(pool, 3, 0)
+        assert e.value.status == L.LORA_ERR_NOT_LOADED
+        L.lora_pool_load(pool, 0, 0, 4, 1.0, h_in, h_out, arr(4, h_in), arr(4, h_out))   # replace
+        assert L.lora_pool_free_pages(pool) == 32
+        L.lora_pool_unload(pool, 0, 0)
+        assert L.lora_pool_free_pages(pool) == 40
+        L.lora_pool_load(pool, 2, 0, 16, 1.0, h_in, h_out, arr(16, h_in), arr(16, h_out))
+        assert L.lora_pool_free_pages(pool) == 8
+    finally:
+        L.lora_pool_destroy(pool)
+
+
+def test_reloaded_pages_serve_the_new_adapter():
+    """Unload + load reuses pages; results follow the newly loaded weights."""
+    w = I.random_case(24, T=50, lengths=[25, 25], n_adapters=2, ranks=[8, 8])
+    with H.DevicePool(w, spare_pages=0) as dp:
+        L.lora_pool_unload(dp.handle, 1, 0)
+        w2 = I.random_case(25, T=50, lengths=[25, 25], n_adapters=2, ranks=[8, 8])
+        at, b = w2.adapter(1)
+        L.lora_pool_load(dp.handle, 1, 0, 8, float(w.scales[1]), 256, 256, H.host_array(at, w.dtype),
+                         H.host_array(b, w.dtype))
+        ss, sa = _tables(w)
+        x = H.to_device(w.x(), w.dtype)
+        y = H.to_device(np.zeros((50, 256), np.float32), w.dtype)
+        v = torch.zeros((50, w.max_rank), dtype=torch.float32, device="cuda")
+        L.lora_sgmv_shrink(dp.handle, 0, x, v, w.max_rank, ss, sa, w.S, w.T)
+        L.lora_sgmv_expand(dp.handle, 0, v, w.max_rank, y, ss, sa, w.S, w.T)
+        assert dp.check_device_status() == 0
+        a0 = w.adapter(0)
+        ad = oracle.Adapters(2, {0: (8, float(w.scales[0]), *a0), 1: (8, float(w.scales[1]), at, b)})
+        from tests.parity import token_ids
+        yr, st = oracle.layer(w.x(), None, token_ids(w), ad, 256)
+        assert st == 0 and rel_err(H.to_host(y), yr) <= TOL_Y[w.dtype]
