@@ -180,6 +180,31 @@ int lora_layer_forward(lora_pool *pool, int matrix, const void *x, const void *W
                        void *workspace, size_t ws_bytes, lora_stream stream);
 
 /*
+ * lora_layer_forward without caller-provided workspace, for callers that
+ * cannot allocate device memory: a serving runtime whose device memory is
+ * carved into a fixed arena at start-up, a decode loop that must not call
+ * cudaMalloc/cudaFree (they synchronise the whole device), or a C plugin with
+ * no allocator of its own.  The pages describe no such variant; it exists
+ * for these callers only.
+ *
+ * Same operation, arguments and errors as lora_layer_forward, minus the
+ * workspace.  The scratch comes from one static device array of
+ * LORA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library keeps until the process exits.  Requires
+ * T * max_rank * 4 <= LORA_NOALLOC_SCRATCH_BYTES (else LORA_ERR_ARG) and the
+ * pool's device to be current (else LORA_ERR_ARG).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  All calls share the array:
+ * calls whose work overlaps on the GPU race and must be serialised by the
+ * caller.  Allocates nothing (no cudaMalloc/cudaFree or allocating library
+ * routine).
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+int lora_layer_forward_noalloc(lora_pool *pool, int matrix, const void *x, const void *W, void *y,
+                               const int *seg_starts, const int *seg_adapter, int S, int T,
+                               lora_stream stream);
+
+/*
  * Synchronise the device, read the pool's device status word into
  * *device_status (may be NULL), and clear it.  Returns LORA_OK when the word
  * was zero, LORA_ERR_DEVICE_INDEX when any LORA_DEV_* bit was set, or

@@ -32,10 +32,12 @@ LORA_DEV_BAD_ADAPTER = 1
 LORA_DEV_BAD_SEGMENTS = 2
 LORA_DEV_WAIT_TIMEOUT = 4
 
+LORA_NOALLOC_SCRATCH_BYTES = 4 << 20
+
 EXPORTS = ["lora_pool_create", "lora_pool_destroy", "lora_pool_load", "lora_pool_unload",
            "lora_pool_free_pages", "lora_sgmv_shrink", "lora_sgmv_expand", "lora_bgmv",
            "lora_layer_forward_workspace_size", "lora_layer_forward", "lora_get_error", "lora_strerror",
-           "lora_launch_count"]
+           "lora_launch_count", "lora_layer_forward_noalloc"]
 
 if not os.path.exists(_build.LIB):
     raise ImportError(f"CUDA library {_build.LIB} is not built: run segmented_gathered_rank_gb300.build.build()")
@@ -64,6 +66,7 @@ _sig("lora_sgmv_expand", _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _P)
 _sig("lora_bgmv", _I, _P, _I, _P, _P, _P, _I, _P)
 _sig("lora_layer_forward_workspace_size", ctypes.c_size_t, _P, _I, _I, _I)
 _sig("lora_layer_forward", _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P, ctypes.c_size_t, _P)
+_sig("lora_layer_forward_noalloc", _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P)
 _sig("lora_get_error", _I, _P, ctypes.POINTER(_I))
 _sig("lora_strerror", ctypes.c_char_p, _I)
 _sig("lora_launch_count", ctypes.c_ulonglong)
@@ -176,6 +179,14 @@ def lora_layer_forward(pool, matrix, x, W, y, seg_starts, seg_adapter, S, T, wor
     _check(_lib.lora_layer_forward(pool, matrix, _dptr(x), _dptr(W), _dptr(y), _dptr(seg_starts),
                                    _dptr(seg_adapter), S, T, _dptr(workspace), ws_bytes, _stream(stream)),
            "lora_layer_forward")
+
+
+def lora_layer_forward_noalloc(pool, matrix, x, W, y, seg_starts, seg_adapter, S, T, stream=None) -> None:
+    """lora_layer_forward with the library's fixed scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check(_lib.lora_layer_forward_noalloc(pool, matrix, _dptr(x), _dptr(W), _dptr(y), _dptr(seg_starts),
+                                           _dptr(seg_adapter), S, T, _stream(stream)),
+           "lora_layer_forward_noalloc")
 
 
 def lora_get_error(pool) -> tuple[int, int]:
