@@ -36,6 +36,7 @@ struct PoolView {
     const int *table;
     int *status;
     long long page_elems;
+    int n_pages;
     int rec_ints;
     int n_matrices;
     int max_adapters;
@@ -64,6 +65,7 @@ struct lora_pool {
     std::vector<int> host_table;      // mirror of the device table
     std::vector<int> mat_h_in;        // per matrix, -1 until the first load
     std::vector<int> mat_h_out;
+    std::vector<int> mat_n_ids;       // per matrix: 1 + largest adapter id ever loaded
     // load staging: pinned host buffer -> device buffer -> scatter kernel
     void *h_stage;
     void *d_stage;
@@ -77,6 +79,7 @@ struct lora_pool {
         v.table = d_table;
         v.status = d_status;
         v.page_elems = page_elems;
+        v.n_pages = n_pages;
         v.rec_ints = rec_ints;
         v.n_matrices = n_matrices;
         v.max_adapters = max_adapters;
@@ -190,6 +193,28 @@ int launch_expand(const lora_pool *pool, int matrix, int h_out, const float *v, 
                   const int *seg_starts, const int *seg_adapter, int S, int T, cudaStream_t st);
 int launch_bgmv(const lora_pool *pool, int matrix, int h_in, int h_out, const void *x, void *y,
                 const int *token_adapter, int T, cudaStream_t st);
+bool bgmv_cluster_ok(const lora_pool *pool, int h_in, int h_out, int T, int n_ids);
+int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, const void *x, void *y,
+                        const int *token_adapter, int T, int n_ids, cudaStream_t st);
+bool sgmv_shrink_ok(const lora_pool *pool, int h_in, int S);
+bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S);
+// plan: nullptr (items from the segment table) or a plan from launch_sgmv_plan
+int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
+                       cudaStream_t st);
+int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
+                       cudaStream_t st);
+// Groups a batch's tokens by adapter into kM-token items (counting sort).
+bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S);
+size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T);
+int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
+                     int *plan, cudaStream_t st);
+bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
+int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
+                   cudaStream_t st);
+int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st);
 int launch_base_gemm(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y,
                      int T, cudaStream_t st);
 

@@ -157,6 +157,9 @@ __global__ void __launch_bounds__(256) base_gemm_simt_kernel(const E *__restrict
 
 int launch_bgmv(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, void *y,
                 const int *token_adapter, int T, cudaStream_t st) {
+    const int n_ids = p->mat_n_ids[matrix];
+    if (bgmv_cluster_ok(p, h_in, h_out, T, n_ids))
+        return launch_bgmv_cluster(p, matrix, h_in, h_out, x, y, token_adapter, T, n_ids, st);
     const size_t smem = (size_t)p->max_rank * sizeof(float);
     if (p->dtype == LORA_BF16)
         bgmv_token_kernel<__nv_bfloat16><<<T, kThreads, smem, st>>>(
@@ -170,6 +173,8 @@ int launch_bgmv(const lora_pool *p, int matrix, int h_in, int h_out, const void 
 
 int launch_shrink(const lora_pool *p, int matrix, int h_in, const void *x, float *v, int ld_v,
                   const int *seg_starts, const int *seg_adapter, int S, int T, cudaStream_t st) {
+    if (sgmv_shrink_ok(p, h_in, S))
+        return launch_sgmv_shrink(p, matrix, h_in, x, v, ld_v, seg_starts, seg_adapter, S, T, nullptr, st);
     const size_t smem = (size_t)p->max_rank * sizeof(float);
     if (p->dtype == LORA_BF16)
         shrink_token_kernel<__nv_bfloat16><<<T, kThreads, smem, st>>>(
@@ -183,6 +188,8 @@ int launch_shrink(const lora_pool *p, int matrix, int h_in, const void *x, float
 
 int launch_expand(const lora_pool *p, int matrix, int h_out, const float *v, int ld_v, void *y,
                   const int *seg_starts, const int *seg_adapter, int S, int T, cudaStream_t st) {
+    if (sgmv_expand_ok(p, h_out, S))
+        return launch_sgmv_expand(p, matrix, h_out, v, ld_v, y, seg_starts, seg_adapter, S, T, nullptr, st);
     const size_t smem = (size_t)p->max_rank * sizeof(float);
     if (p->dtype == LORA_BF16)
         expand_token_kernel<__nv_bfloat16><<<T, kThreads, smem, st>>>(

@@ -76,9 +76,6 @@ extern "C" int lora_layer_forward_noalloc(lora_pool *p, int matrix, const void *
     if (device != p->device) return LORA_ERR_ARG;
     void *scratch = nullptr;
     if ((rc = scratch_address(device, &scratch))) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    float *v = static_cast<float *>(scratch);
-    if ((rc = launch_base_gemm(p, h_in, h_out, x, W, y, T, st))) return rc;
-    if ((rc = launch_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, st))) return rc;
-    return launch_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, st);
+    return layer_forward_impl(p, matrix, h_in, h_out, x, W, y, seg_starts, seg_adapter, S, T,
+                              static_cast<float *>(scratch), (cudaStream_t)stream);
 }

@@ -55,6 +55,29 @@ __global__ void set_rank_kernel(int *table, long long rec_off, int rank) { table
 
 }  // namespace lora
 
+namespace lora {
+// The adapted layer given scratch for v (T x max_rank fp32): base product for
+// the whole batch (tensor cores when the shape allows), then each token's own
+// low-rank term: shrink into v, expand into y.
+int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st) {
+    int rc = gemm_tc_ok(p, h_in, h_out, T) ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st)
+                                           : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+    if (rc) return rc;
+    if (sgmv_plan_ok(p, matrix, S) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
+        // tokens grouped by adapter (plan in the workspace, after v), then shrink and expand per group
+        int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
+                                            ~uintptr_t(255));
+        if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st))) return rc;
+        if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st)))
+            return rc;
+        return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st);
+    }
+    if ((rc = launch_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, st))) return rc;
+    return launch_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, st);
+}
+}  // namespace lora
+
 using namespace lora;
 
 extern "C" {
@@ -122,6 +145,7 @@ int lora_pool_create(lora_pool **out, int dtype, int page_elems, int n_pages, in
         p->host_table.assign(n_rec * p->rec_ints, -1);
         p->mat_h_in.assign(n_matrices, -1);
         p->mat_h_out.assign(n_matrices, -1);
+        p->mat_n_ids.assign(n_matrices, 0);
     } catch (...) {
         lora_pool_destroy(p);
         return LORA_ERR_ARG;
@@ -218,6 +242,7 @@ int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale,
     for (int i = 0; i < 2 * rank; ++i) hrec[kRecHeader + i] = la->ids[i];
     p->mat_h_in[matrix] = h_in;
     p->mat_h_out[matrix] = h_out;
+    if (adapter + 1 > p->mat_n_ids[matrix]) p->mat_n_ids[matrix] = adapter + 1;
     return LORA_OK;
 }
 
@@ -294,7 +319,7 @@ int lora_bgmv(lora_pool *p, int matrix, const void *x, void *y, const int *token
 size_t lora_layer_forward_workspace_size(const lora_pool *p, int matrix, int S, int T) {
     int h_in, h_out;
     if (!p || T < 0 || S < 0 || matrix_dims(p, matrix, &h_in, &h_out)) return 0;
-    return (size_t)T * p->max_rank * sizeof(float) + 256;
+    return (size_t)T * p->max_rank * sizeof(float) + sgmv_plan_bytes(p, matrix, T) + 256;
 }
 
 int lora_layer_forward(lora_pool *p, int matrix, const void *x, const void *W, void *y,
@@ -309,11 +334,8 @@ int lora_layer_forward(lora_pool *p, int matrix, const void *x, const void *W, v
         !aligned16(y) || !aligned16(workspace))
         return LORA_ERR_ARG;
     if (ws_bytes < lora_layer_forward_workspace_size(p, matrix, S, T)) return LORA_ERR_ARG;
-    cudaStream_t st = (cudaStream_t)stream;
-    float *v = (float *)workspace;
-    if ((rc = launch_base_gemm(p, h_in, h_out, x, W, y, T, st))) return rc;
-    if ((rc = launch_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, st))) return rc;
-    return launch_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, st);
+    return layer_forward_impl(p, matrix, h_in, h_out, x, W, y, seg_starts, seg_adapter, S, T,
+                              static_cast<float *>(workspace), (cudaStream_t)stream);
 }
 
 }  // extern "C"

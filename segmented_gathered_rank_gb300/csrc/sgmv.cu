@@ -1,0 +1,651 @@
+// SGMV for prefill: "segmented gather, for contiguous segments of tokens
+// sharing an adapter" ("Multi-LoRA Serving", section "The kernel trick:
+// gather, do not merge"), with per-adapter ranks (S-LoRA slide 10, MBGMM).
+//
+//   shrink:  v[t][j]  = sum_k x[t][k] * A_T_a[j][k]            j < r_a
+//   expand:  y[t][n] += s_a * sum_j v[t][j] * B_a[j][n]
+//
+// Work items are one adapter and up to kM of its tokens.  They come either
+// from the segment table (each segment cut into kM-token chunks; every CTA
+// finds its item with a block-wide scan of chunk counts and a binary search,
+// so Zipf-skewed segment lengths spread over as many CTAs as they have
+// chunks), or from a plan built by sgmv_plan_kernel, which groups the tokens
+// of a batch by adapter with a counting sort (so a decode batch whose tokens
+// are one-token segments still gets items of up to kM tokens).
+//
+// Adapter pages, x and y move with 16-byte asynchronous copies through
+// multi-stage shared-memory pipelines; the products run on the tensor cores
+// as warp-level mma.sync m16n8k16 (bf16 -> fp32) -- tiles here are 32
+// tokens by at most a few dozen ranks, and the kernels are bound by HBM
+// traffic, not MMA rate.  In the expand, v enters the MMA as a bf16 high part
+// plus a bf16 residual, which keeps the product within fp32-level error.
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace lora {
+namespace {
+
+constexpr int kM = 32;            // tokens per item
+constexpr int kKs = 128;          // k per shrink pipeline stage
+constexpr int kStagesS = 4;
+constexpr int kNb = 128;          // output columns per expand block
+constexpr int kBlocksPerUnit = 4; // column blocks per expand unit (512 columns)
+constexpr int kStagesE = 3;
+constexpr int kMaxS = 8192;       // segments the segment-mode kernels take
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma16816(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ int clamp_page(const PoolView &pv, int id) {
+    return id < 0 ? 0 : (id >= pv.n_pages ? pv.n_pages - 1 : id);
+}
+
+// Exclusive scan of v[0..n) in place by a block of NT threads; returns the total.
+template <int NT>
+__device__ int block_scan(int *v, int n, int *wtot) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + NT - 1) / NT;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += v[i];
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) wtot[warp] = inc;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int t = wtot[w];
+            wtot[w] = run;
+            run += t;
+        }
+        wtot[NW] = run;
+    }
+    __syncthreads();
+    int run = wtot[warp] + inc - sum;
+    for (int i = lo; i < hi; ++i) {
+        const int t = v[i];
+        v[i] = run;
+        run += t;
+    }
+    const int total = wtot[NW];
+    __syncthreads();
+    return total;
+}
+
+// An item: adapter `a` and its tokens; row i of the item is token
+// perm ? perm[off + i] : off + i.
+struct Item {
+    int a;
+    int off;
+    int nt;
+    int pad;
+};
+
+// Item `idx` among the (segment, kM-token chunk) pairs of a segment table.
+// scan: S + 1 ints of shared memory; wtot: NT/32 + 4 ints.  All threads return it.
+template <int NT>
+__device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int S, int T, int idx, int *scan,
+                             int *wtot) {
+    for (int s = threadIdx.x; s < S; s += NT) {
+        const int a = min(max(seg_starts[s], 0), T), b = min(max(seg_starts[s + 1], 0), T);
+        scan[s] = b > a ? (b - a + kM - 1) / kM : 0;
+    }
+    __syncthreads();
+    const int total = block_scan<NT>(scan, S, wtot);
+    if (threadIdx.x == 0) {
+        Item it{-1, 0, 0, 0};
+        if (idx < total) {
+            int lo = 0, hi = S - 1;               // last segment whose first chunk index <= idx
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (scan[mid] <= idx) lo = mid; else hi = mid - 1;
+            }
+            const int c = idx - scan[lo];
+            const int beg = min(max(seg_starts[lo], 0), T), end = min(max(seg_starts[lo + 1], 0), T);
+            it.a = seg_adapter[lo];
+            it.off = beg + c * kM;
+            it.nt = min(kM, end - it.off);
+        }
+        reinterpret_cast<Item *>(wtot)[0] = it;
+    }
+    __syncthreads();
+    const Item it = reinterpret_cast<Item *>(wtot)[0];
+    __syncthreads();
+    return it;
+}
+
+// The work items of one launch: from a plan (if given) or from the segment table.
+struct ItemSource {
+    const int *seg_starts, *seg_adapter;
+    int S, T;
+    const int *plan;     // nullptr, or [n_items, pad x3, perm[T], items[...] as Item]
+};
+
+__device__ __forceinline__ const int *plan_perm(const int *plan) { return plan + 4; }
+__device__ __forceinline__ const Item *plan_items(const int *plan, int T) {
+    return reinterpret_cast<const Item *>(plan + 4 + ((T + 3) & ~3));
+}
+
+template <int NT>
+__device__ Item get_item(const ItemSource &src, int idx, int *scan, int *wtot) {
+    if (src.plan) {
+        if (idx >= src.plan[0]) return Item{-1, 0, 0, 0};
+        return plan_items(src.plan, src.T)[idx];
+    }
+    return segment_item<NT>(src.seg_starts, src.seg_adapter, src.S, src.T, idx, scan, wtot);
+}
+
+// Record of adapter a on matrix m into smem; false (after flagging) when invalid.
+template <int NT>
+__device__ bool load_record(const PoolView &pv, int a, int m, int *rec, bool report) {
+    if (a >= pv.max_adapters) {
+        if (report) flag(pv.status, LORA_DEV_BAD_ADAPTER);
+        return false;
+    }
+    for (int i = threadIdx.x; i < pv.rec_ints; i += NT)
+        rec[i] = pv.table[((long long)a * pv.n_matrices + m) * pv.rec_ints + i];
+    __syncthreads();
+    if (rec[0] < 0) {
+        if (report) flag(pv.status, LORA_DEV_BAD_ADAPTER);
+        return false;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Plan: tokens grouped by adapter (counting sort), cut into kM-token items.
+// ---------------------------------------------------------------------------
+struct PlanParams {
+    const int *seg_starts, *seg_adapter;
+    int S, T;
+    int n_ids;          // adapter ids below this may be loaded on the matrix
+    int *status;
+    int *plan;          // output, see ItemSource
+    int max_items;
+};
+
+__global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
+    extern __shared__ int sm[];
+    int *cnt = sm;                       // [n_ids] tokens per adapter
+    int *base = cnt + p.n_ids;           // [n_ids] token offset of each adapter
+    int *ibase = base + p.n_ids;         // [n_ids] item offset of each adapter
+    int *segoff = ibase + p.n_ids;       // [S] offset of each segment within its adapter's tokens
+    int *sb = segoff + p.S;              // [S + 1] segment bounds, clamped into [0, T]
+    int *sa = sb + p.S + 1;              // [S] segment adapters (-1: none or invalid)
+    int *wtot = sa + p.S;                // [kPlanThreads / 32 + 1]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int nwarps = kPlanThreads / 32;
+    if (tid == 0) check_segments(p.seg_starts, p.S, p.T, p.status);
+    for (int i = tid; i < p.n_ids; i += kPlanThreads) cnt[i] = 0;
+    for (int s = tid; s <= p.S; s += kPlanThreads) sb[s] = min(max(p.seg_starts[s], 0), p.T);
+    for (int s = tid; s < p.S; s += kPlanThreads) {
+        const int a = p.seg_adapter[s];
+        sa[s] = a < p.n_ids ? a : -1;
+        if (a >= p.n_ids) flag(p.status, LORA_DEV_BAD_ADAPTER);      // never loaded on this matrix
+    }
+    __syncthreads();
+    // one atomic per segment: its tokens stay contiguous and in order
+    for (int s = tid; s < p.S; s += kPlanThreads) {
+        const int n = sb[s + 1] - sb[s];
+        segoff[s] = (sa[s] >= 0 && n > 0) ? atomicAdd(&cnt[sa[s]], n) : -1;
+    }
+    __syncthreads();
+    for (int i = tid; i < p.n_ids; i += kPlanThreads) {
+        base[i] = cnt[i];
+        ibase[i] = (cnt[i] + kM - 1) / kM;
+    }
+    __syncthreads();
+    block_scan<kPlanThreads>(base, p.n_ids, wtot);
+    const int n_items = block_scan<kPlanThreads>(ibase, p.n_ids, wtot);
+    int *perm = p.plan + 4;
+    Item *items = reinterpret_cast<Item *>(p.plan + 4 + ((p.T + 3) & ~3));
+    for (int a = tid; a < p.n_ids; a += kPlanThreads) {
+        const int n = cnt[a];
+        for (int c = 0; c * kM < n; ++c) {
+            // an invalid (overlapping) segment table can count more than T tokens: never point past T
+            const int off = base[a] + c * kM;
+            const int nt = max(0, min(min(kM, n - c * kM), p.T - off));
+            if (ibase[a] + c < p.max_items) items[ibase[a] + c] = Item{nt > 0 ? a : -1, off, nt, 0};
+        }
+    }
+    if (tid == 0) p.plan[0] = min(n_items, p.max_items);
+    // token permutation: short segments one per thread, long ones one per warp
+    for (int s = tid; s < p.S; s += kPlanThreads) {
+        const int n = sb[s + 1] - sb[s];
+        if (segoff[s] < 0 || n > 32) continue;
+        const int dst = base[sa[s]] + segoff[s];
+        for (int i = 0; i < n; ++i)
+            if (dst + i < p.T) perm[dst + i] = sb[s] + i;
+    }
+    for (int s = warp; s < p.S; s += nwarps) {
+        const int n = sb[s + 1] - sb[s];
+        if (segoff[s] < 0 || n <= 32) continue;
+        const int dst = base[sa[s]] + segoff[s];
+        for (int i = lane; i < n; i += 32)
+            if (dst + i < p.T) perm[dst + i] = sb[s] + i;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shrink: 128 threads, 32 tokens x (ranks) per item, K in 128-wide stages.
+// warp w: rows 16*(w & 1) .. +16, k half (w >> 1) of each stage.
+// ---------------------------------------------------------------------------
+constexpr int kThreadsS = 128;
+
+struct ShrinkParams {
+    PoolView pv;
+    ItemSource src;
+    int m, h_in;
+    int npc;       // ranks per CTA: max_rank rounded up to 16, at most 32 (grid.y covers the rest)
+    const __nv_bfloat16 *x;
+    float *v;
+    int ld_v;
+};
+
+__global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int pitch = kKs + 8;                                        // bf16 per smem row
+    const int npc = p.npc;
+    __nv_bfloat16 *sx = reinterpret_cast<__nv_bfloat16 *>(smem_raw);     // [stages][kM][pitch]
+    __nv_bfloat16 *sa = sx + kStagesS * kM * pitch;                      // [stages][npc][pitch]
+    float *red = reinterpret_cast<float *>(sa + kStagesS * npc * pitch);  // [2][16][npc]
+    int *tok = reinterpret_cast<int *>(red + 2 * 16 * npc);              // [kM]
+    int *wtot = tok + kM;                                                // [8]
+    int *rec = wtot + 8;                                                 // [rec_ints]
+    int *scan = rec + p.pv.rec_ints;                                     // [S + 1]
+
+    if (blockIdx.x == 0 && tid == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    const Item it = get_item<kThreadsS>(p.src, blockIdx.x, scan, wtot);
+    if (it.a < 0 || it.nt <= 0) return;
+    if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0)) return;
+    if ((int)blockIdx.y * p.npc >= min(rec[0], min(p.pv.max_rank, p.ld_v))) return;
+    if (tid < kM)
+        tok[tid] = tid < it.nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
+                               : 0;
+    __syncthreads();
+
+    const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
+    const int mg = warp & 1, kh = warp >> 1;
+    const int g = lane >> 2, q = lane & 3;
+    const int nk = p.h_in / kKs;
+
+    // this CTA's ranks: chunk blockIdx.y of npc (ranks above an adapter's own are not its work)
+    for (int j0 = blockIdx.y * npc; j0 < min(r, (int)(blockIdx.y + 1) * npc); j0 += npc) {
+        const int np = min(npc, r - j0);
+        const int npad = (np + 15) & ~15;
+        // rows that never receive copies stay zero for the whole pass
+        for (int i = tid; i < kStagesS * kM * (pitch / 8); i += kThreadsS)
+            if ((i / (pitch / 8)) % kM >= it.nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < kStagesS * npc * (pitch / 8); i += kThreadsS)
+            if ((i / (pitch / 8)) % npc >= np) reinterpret_cast<uint4 *>(sa)[i] = make_uint4(0, 0, 0, 0);
+        auto issue = [&](int kc) {
+            const int st = kc % kStagesS;
+            __nv_bfloat16 *dx = sx + st * kM * pitch;
+            __nv_bfloat16 *da = sa + st * npc * pitch;
+            for (int i = tid; i < it.nt * (kKs / 8); i += kThreadsS) {
+                const int row = i >> 4, kv = i & 15;
+                cp_async16(dx + row * pitch + kv * 8, p.x + (long long)tok[row] * p.h_in + kc * kKs + kv * 8);
+            }
+            for (int i = tid; i < np * (kKs / 8); i += kThreadsS) {
+                const int row = i >> 4, kv = i & 15;
+                const int page = clamp_page(p.pv, rec[kRecHeader + j0 + row]);
+                cp_async16(da + row * pitch + kv * 8, page_row<__nv_bfloat16>(p.pv, page) + kc * kKs + kv * 8);
+            }
+        };
+        float d[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+#pragma unroll
+        for (int kc = 0; kc < kStagesS - 1; ++kc) {
+            if (kc < nk) issue(kc);
+            cp_commit();
+        }
+        for (int kc = 0; kc < nk; ++kc) {
+            cp_wait<kStagesS - 2>();
+            __syncthreads();
+            if (kc + kStagesS - 1 < nk) issue(kc + kStagesS - 1);
+            cp_commit();
+            const int st = kc % kStagesS;
+            const __nv_bfloat16 *bx = sx + st * kM * pitch;
+            const __nv_bfloat16 *ba = sa + st * npc * pitch;
+#pragma unroll
+            for (int ks = 0; ks < kKs / 32; ++ks) {           // this warp's half of the stage
+                const int k = kh * (kKs / 2) + ks * 16;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(bx + (mg * 16 + (lane & 15)) * pitch + k + (lane >> 4) * 8, a0, a1, a2, a3);
+#pragma unroll
+                for (int t = 0; t < 8; t += 2) {
+                    if (t * 8 >= npad) break;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(ba + (t * 8 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k + ((lane >> 3) & 1) * 8, b0,
+                            b1, b2, b3);
+                    mma16816(d[t], a0, a1, a2, a3, b0, b1);
+                    mma16816(d[t + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+        }
+        cp_wait<0>();
+        __syncthreads();
+        // combine the two k halves and write v
+        float *rw = red + mg * 16 * npc;
+        if (kh == 1) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t * 8 >= npad) break;
+                rw[g * npc + t * 8 + 2 * q] = d[t][0];
+                rw[g * npc + t * 8 + 2 * q + 1] = d[t][1];
+                rw[(g + 8) * npc + t * 8 + 2 * q] = d[t][2];
+                rw[(g + 8) * npc + t * 8 + 2 * q + 1] = d[t][3];
+            }
+        }
+        __syncthreads();
+        if (kh == 0) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t * 8 >= npad) break;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = mg * 16 + g + 8 * h;
+                    const int j = t * 8 + 2 * q;
+                    if (row >= it.nt) continue;
+                    float *vrow = p.v + (long long)tok[row] * p.ld_v + j0;
+                    const float v0 = d[t][2 * h] + rw[(g + 8 * h) * npc + j];
+                    const float v1 = d[t][2 * h + 1] + rw[(g + 8 * h) * npc + j + 1];
+                    if (j < np) vrow[j] = v0;
+                    if (j + 1 < np) vrow[j + 1] = v1;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Expand: 128 threads, unit = (item, up to kBlocksPerUnit column blocks of
+// kNb).  warp w: rows 16*(w & 1) .. +16, columns 64*(w >> 1) .. +64 of the
+// block.  y tiles and B chunks stream through a 3-stage pipeline; y is read
+// and written with coalesced 16-byte accesses staged in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kThreadsE = 128;
+
+struct ExpandParams {
+    PoolView pv;
+    ItemSource src;
+    int m, h_out;
+    int kpc;       // ranks per pass: max_rank rounded up to 16, at most 64
+    const float *v;
+    int ld_v;
+    __nv_bfloat16 *y;
+    int ncg;       // column groups per item
+};
+
+__global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int yp = kNb + 8;                  // bf16 per smem row of y and B tiles
+    const int kpc = p.kpc, vp = p.kpc + 8;
+    __nv_bfloat16 *sy = reinterpret_cast<__nv_bfloat16 *>(smem_raw);      // [stages][kM][yp]
+    __nv_bfloat16 *sb = sy + kStagesE * kM * yp;                          // [stages][kpc][yp]
+    __nv_bfloat16 *svh = sb + kStagesE * kpc * yp;                        // [kM][vp]
+    __nv_bfloat16 *svl = svh + kM * vp;                                   // [kM][vp]
+    int *tok = reinterpret_cast<int *>(svl + kM * vp);                    // [kM]
+    int *wtot = tok + kM;                                                 // [8]
+    int *rec = wtot + 8;
+    int *scan = rec + p.pv.rec_ints;
+
+    if (blockIdx.x == 0 && tid == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    const int cg = blockIdx.x % p.ncg;
+    const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
+    if (it.a < 0 || it.nt <= 0) return;
+    if (!load_record<kThreadsE>(p.pv, it.a, p.m, rec, tid == 0 && cg == 0)) return;
+    if (tid < kM)
+        tok[tid] = tid < it.nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
+                               : 0;
+    __syncthreads();
+    const int r_rec = min(rec[0], p.pv.max_rank);
+    const int r = min(r_rec, p.ld_v);
+    const float scale = __int_as_float(rec[1]);
+    const int nb_total = (p.h_out + kNb - 1) / kNb;
+    const int b_first = cg * kBlocksPerUnit;
+    const int nb = min(kBlocksPerUnit, nb_total - b_first);
+    if (nb <= 0 || r <= 0) return;
+    const int mg = warp & 1, nh = warp >> 1;
+    const int g = lane >> 2, q = lane & 3;
+
+    // ranks in passes of kpc; each pass streams the unit's y blocks once
+    for (int j0 = 0; j0 < r; j0 += kpc) {
+        const int rn = min(kpc, r - j0);
+        const int kpad = (rn + 15) & ~15;
+        auto issue = [&](int bi) {
+            const int st = bi % kStagesE;
+            const int n0 = (b_first + bi) * kNb;
+            const int ncv = min(kNb, p.h_out - n0) / 8;
+            __nv_bfloat16 *dy = sy + st * kM * yp;
+            __nv_bfloat16 *db = sb + st * kpc * yp;
+            for (int i = tid; i < it.nt * (kNb / 8); i += kThreadsE) {
+                const int row = i >> 4, cv = i & 15;
+                if (cv < ncv) cp_async16(dy + row * yp + cv * 8, p.y + (long long)tok[row] * p.h_out + n0 + cv * 8);
+            }
+            for (int i = tid; i < kpad * (kNb / 8); i += kThreadsE) {
+                const int row = i >> 4, cv = i & 15;
+                __nv_bfloat16 *dst = db + row * yp + cv * 8;
+                if (row < rn && cv < ncv) {
+                    const int page = clamp_page(p.pv, rec[kRecHeader + r_rec + j0 + row]);
+                    cp_async16(dst, page_row<__nv_bfloat16>(p.pv, page) + n0 + cv * 8);
+                } else {
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        };
+#pragma unroll
+        for (int bi = 0; bi < kStagesE - 1; ++bi) {
+            if (bi < nb) issue(bi);
+            cp_commit();
+        }
+        // v of the item's tokens for this pass, scaled, as two bf16 parts (rows past the item are zero)
+        for (int i = tid; i < kM * kpad; i += kThreadsE) {
+            const int row = i / kpad, j = i % kpad;
+            float val = 0.f;
+            if (row < it.nt && j < rn) val = scale * p.v[(long long)tok[row] * p.ld_v + j0 + j];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+            svh[row * vp + j] = hi;
+            svl[row * vp + j] = __float2bfloat16_rn(val - __bfloat162float(hi));
+        }
+
+        for (int bi = 0; bi < nb; ++bi) {
+            cp_wait<kStagesE - 2>();
+            __syncthreads();
+            if (bi + kStagesE - 1 < nb) issue(bi + kStagesE - 1);
+            cp_commit();
+            const int st = bi % kStagesE;
+            __nv_bfloat16 *ty = sy + st * kM * yp;
+            const __nv_bfloat16 *tb = sb + st * kpc * yp;
+            float d[8][4];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+            for (int kk = 0; kk < kpad; kk += 16) {
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                ldsm_x4(svh + (mg * 16 + (lane & 15)) * vp + kk + (lane >> 4) * 8, h0, h1, h2, h3);
+                ldsm_x4(svl + (mg * 16 + (lane & 15)) * vp + kk + (lane >> 4) * 8, l0, l1, l2, l3);
+#pragma unroll
+                for (int t = 0; t < 8; t += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(tb + (kk + (lane & 7) + ((lane >> 3) & 1) * 8) * yp + nh * 64 + (t + (lane >> 4)) * 8,
+                              b0, b1, b2, b3);
+                    mma16816(d[t], h0, h1, h2, h3, b0, b1);
+                    mma16816(d[t], l0, l1, l2, l3, b0, b1);
+                    mma16816(d[t + 1], h0, h1, h2, h3, b2, b3);
+                    mma16816(d[t + 1], l0, l1, l2, l3, b2, b3);
+                }
+            }
+            // y tile += delta in shared memory, then coalesced stores
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = mg * 16 + g + 8 * h;
+                    __nv_bfloat162 *yy =
+                        reinterpret_cast<__nv_bfloat162 *>(ty + row * yp + nh * 64 + t * 8 + 2 * q);
+                    const float2 f = __bfloat1622float2(*yy);
+                    *yy = __floats2bfloat162_rn(f.x + d[t][2 * h], f.y + d[t][2 * h + 1]);
+                }
+            __syncthreads();
+            const int n0 = (b_first + bi) * kNb;
+            const int ncv = min(kNb, p.h_out - n0) / 8;
+            for (int i = tid; i < it.nt * (kNb / 8); i += kThreadsE) {
+                const int row = i >> 4, cv = i & 15;
+                if (cv < ncv)
+                    *reinterpret_cast<uint4 *>(p.y + (long long)tok[row] * p.h_out + n0 + cv * 8) =
+                        *reinterpret_cast<const uint4 *>(ty + row * yp + cv * 8);
+            }
+        }
+        cp_wait<0>();
+        __syncthreads();   // this pass's stores are issued before the next pass reloads y
+    }
+}
+
+// Upper bound on items: every non-empty segment (or adapter) has at least
+// one chunk, and the chunks together cover T tokens.
+int item_bound(int groups, int T) { return std::min(groups, T) + (T + kM - 1) / kM; }
+
+}  // namespace
+
+bool sgmv_shrink_ok(const lora_pool *pool, int h_in, int S) {
+    return pool->dtype == LORA_BF16 && h_in % kKs == 0 && S <= kMaxS;
+}
+
+bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S) {
+    return pool->dtype == LORA_BF16 && h_out % 8 == 0 && S <= kMaxS;
+}
+
+size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T) {
+    const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
+    return (size_t)(4 + ((T + 3) & ~3)) * 4 + (size_t)item_bound(n_ids, T) * sizeof(Item) + 64;
+}
+
+bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S) {
+    const int n_ids = pool->mat_n_ids[matrix];
+    return n_ids > 0 && S <= kMaxS && (size_t)(3 * n_ids + 3 * S) * 4 + 256 <= 160 * 1024;
+}
+
+int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
+                     int *plan, cudaStream_t st) {
+    PlanParams p;
+    p.seg_starts = seg_starts;
+    p.seg_adapter = seg_adapter;
+    p.S = S;
+    p.T = T;
+    p.n_ids = pool->mat_n_ids[matrix];
+    p.status = pool->d_status;
+    p.plan = plan;
+    p.max_items = item_bound(p.n_ids, T);
+    const size_t smem = (size_t)(3 * p.n_ids + 3 * S + 1 + kPlanThreads / 32 + 2) * 4;
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(sgmv_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        configured = smem;
+    }
+    sgmv_plan_kernel<<<1, kPlanThreads, smem, st>>>(p);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
+                       cudaStream_t st) {
+    ShrinkParams p;
+    p.pv = pool->view();
+    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
+    p.m = matrix;
+    p.h_in = h_in;
+    p.npc = std::min(32, (pool->max_rank + 15) / 16 * 16);
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.v = v;
+    p.ld_v = ld_v;
+    const size_t smem = (size_t)kStagesS * (kM + p.npc) * (kKs + 8) * 2 + (size_t)2 * 16 * p.npc * 4 +
+                        (size_t)(kM + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(sgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        configured = smem;
+    }
+    const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
+    const dim3 grid(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc);
+    sgmv_shrink_kernel<<<grid, kThreadsS, smem, st>>>(p);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
+                       const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
+                       cudaStream_t st) {
+    ExpandParams p;
+    p.pv = pool->view();
+    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
+    p.m = matrix;
+    p.h_out = h_out;
+    p.kpc = std::min(64, (pool->max_rank + 15) / 16 * 16);
+    p.v = v;
+    p.ld_v = ld_v;
+    p.y = static_cast<__nv_bfloat16 *>(y);
+    const int nb_total = (h_out + kNb - 1) / kNb;
+    p.ncg = (nb_total + kBlocksPerUnit - 1) / kBlocksPerUnit;
+    const size_t smem = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
+                        (size_t)(kM + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(sgmv_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        configured = smem;
+    }
+    const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
+    sgmv_expand_kernel<<<item_bound(groups, T) * p.ncg, kThreadsE, smem, st>>>(p);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace lora

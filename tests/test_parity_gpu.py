@@ -359,3 +359,25 @@ def test_reloaded_pages_serve_the_new_adapter():
         from tests.parity import token_ids
         yr, st = oracle.layer(w.x(), None, token_ids(w), ad, 256)
         assert st == 0 and rel_err(H.to_host(y), yr) <= TOL_Y[w.dtype]
+
+
+def test_bgmv_zipf_decode_hot_rank128_adapter():
+    """The fused-layer workload's 512 decode tokens alone: Zipf(1.0) ids over
+    128 adapters, adapter 0 (the hottest) at rank 128 -- many tokens per
+    adapter and ranks above one chunk."""
+    import dataclasses
+    w = I.fused_layer()
+    ids = w.seg_adapter[4:].copy()
+    wd = dataclasses.replace(w, T=512, seg_starts=np.arange(513, dtype=np.int32), seg_adapter=ids,
+                             token_adapter=ids.copy())
+    assert (ids == 0).sum() > 16
+    for m in (0, 1):
+        check_bgmv(wd, m)
+
+
+def test_bgmv_all_tokens_one_adapter_and_none():
+    w = I.random_case(31, T=200, decode=True, n_adapters=3, ranks=[32, 8, 16], h_in=512, h_out=512)
+    w.token_adapter[:] = 1
+    w.token_adapter[::7] = -1
+    w.seg_adapter = w.token_adapter.copy()
+    check_bgmv(w)
