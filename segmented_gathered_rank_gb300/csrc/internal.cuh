@@ -30,6 +30,12 @@ namespace lora {
 
 constexpr int kRecHeader = 4;
 
+// The tensor-core GEMM adds the adapter term itself for an M-tile of
+// kFuseTileRows rows that all use one adapter of rank <= kFuseMaxRank (in
+// 64-rank rounds); the plan marks such tiles and the expand skips their rows.
+constexpr int kFuseTileRows = 128;
+constexpr int kFuseMaxRank = 128;
+
 // Everything a kernel needs to resolve (adapter, matrix) -> rows of pages.
 struct PoolView {
     void *pages;
@@ -177,11 +183,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Checks a device segment table (one thread); sets LORA_DEV_BAD_SEGMENTS.
+// Checks a device segment table; every thread of the block calls it (the
+// starts are read in parallel, then OR-reduced).  Sets LORA_DEV_BAD_SEGMENTS.
 __device__ __forceinline__ void check_segments(const int *seg_starts, int S, int T, int *status) {
-    bool bad = seg_starts[0] != 0 || seg_starts[S] != T;
-    for (int s = 0; s < S && !bad; ++s) bad = seg_starts[s + 1] < seg_starts[s];
-    if (bad) flag(status, LORA_DEV_BAD_SEGMENTS);
+    bool bad = threadIdx.x == 0 && (seg_starts[0] != 0 || seg_starts[S] != T);
+    for (int s = threadIdx.x; s < S; s += blockDim.x) bad |= seg_starts[s + 1] < seg_starts[s];
+    if (__syncthreads_or(bad) && threadIdx.x == 0) flag(status, LORA_DEV_BAD_SEGMENTS);
 }
 
 // ---------------------------------------------------------------------------
@@ -204,15 +211,21 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
                        cudaStream_t st);
 int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
-                       cudaStream_t st);
+                       cudaStream_t st, const int *tile_ad = nullptr);
 // Groups a batch's tokens by adapter into kM-token items (counting sort).
 bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S);
 size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T);
+// The plan's per-M-tile array (after its items).
+int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan);
+// tile_ad != nullptr: also classify the GEMM's 128-row M-tiles (see launch_gemm_tc).
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                     int *plan, cudaStream_t st);
+                     int *plan, cudaStream_t st, int *tile_ad = nullptr);
 bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
+// tile_ad != nullptr: M-tiles with tile_ad[m] >= 0 also get that adapter's term
+// s * v . B (v: T x ld_v fp32 from the shrink) inside the GEMM.
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
-                   cudaStream_t st);
+                   cudaStream_t st, int matrix = 0, const int *tile_ad = nullptr, const float *v = nullptr,
+                   int ld_v = 0);
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st);
 int launch_base_gemm(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y,

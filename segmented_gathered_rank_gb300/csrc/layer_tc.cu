@@ -29,62 +29,167 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = kFuseTileRows, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreadsTC = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
+
+constexpr int A2_BYTES = BM * 64 * 2;   // s * v tile, one 64-wide K chunk (high or residual part)
+constexpr int B2_BYTES = BN * 64 * 2;   // B rows of the tile's columns, transposed to K-major
 
 struct LayerTcParams {
     int T, N, K;
     int num_m, num_n, num_k, num_tiles;
     __nv_bfloat16 *y;
     int *status;
+    // adapter term for uniform M-tiles (fused variant only)
+    const int *tile_ad;     // per M-tile: adapter whose term is added here, or -1
+    PoolView pv;
+    int m;
+    const float *v;
+    int ld_v;
 };
 
+template <int ST>
 struct Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[ST];
+    uint64_t empty[ST];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t aready;      // one 64-rank round of a tile's adapter operands is in shared memory
+    uint64_t aconsumed;   // the MMAs of that round have read it
     uint32_t tmem_base;
     int abort;
+    int akpad;            // K of the staged round (0: the tile has no adapter term)
+    int arounds;          // rounds of that tile (set with round 0)
 };
 
-__device__ __forceinline__ unsigned long long now_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-    return t;
+// Byte offset of 16-byte chunk c of row `row` in a K-major tile with 128-byte
+// swizzling (8-row, 1024-byte atoms; chunk index XOR row-in-atom) -- the
+// layout TMA writes and the UMMA descriptor reads.
+__device__ __forceinline__ uint32_t swz128(int row, int c) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + (((c ^ row) & 7) << 4));
 }
 
-// Bounded wait on one phase; gives up after kTimeoutNs or when *abort is set.
-__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    const unsigned long long t0 = now_ns();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
-            if (abort && *abort) return false;
-            if (now_ns() - t0 > kTimeoutNs) return false;
+// Epilogue warps (128 threads): stage round `round` (ranks 64*round ..
+// 64*round+63) of the adapter term's operands of `tile`; returns the tile's
+// number of rounds.  A2hi/A2lo: s * v of the tile's rows (bf16 high part /
+// residual), K-major; B2: row n holds B_a[j][n0 + n] (the B rows transposed),
+// K-major.  Every global load of a round is independent of the others but
+// for the page ids, so a round costs about two memory round trips.
+template <int ST>
+__device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t *a2hi, uint8_t *a2lo, uint8_t *b2,
+                            Ctrl<ST> *ctrl, int ethr) {
+    const int mb = tile % p.num_m, nb = tile / p.num_m;
+    const int a = p.tile_ad[mb];
+    int r = 0;
+    const int *rec = nullptr;
+    if (a >= 0 && a < p.pv.max_adapters) {
+        rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
+        r = rec[0];
+        if (r < 1 || r > kFuseMaxRank || r > p.ld_v) r = 0;
+    }
+    const int rounds = (r + 63) / 64;
+    const int j0 = round * 64, rn = max(0, min(64, r - j0));
+    const int kpad = (rn + 15) & ~15;
+    if (ethr == 0) {
+        ctrl->akpad = kpad;
+        if (round == 0) ctrl->arounds = rounds;
+    }
+    if (kpad == 0) return rounds;
+    const float s = __int_as_float(rec[1]);
+    const int lane = ethr & 31, w = ethr >> 5;
+    // B page ids of this lane's ranks (lane, lane + 32)
+    int page[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        int pg = j < rn ? rec[kRecHeader + r + j0 + j] : 0;
+        page[h] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
+    }
+    // A2: row ethr of the tile, s * v split into bf16 high part and residual
+    {
+        const int row = mb * BM + ethr;
+        const bool live = row < p.T;
+        const float *vrow = p.v + (long long)(live ? row : 0) * p.ld_v + j0;
+        float vv[64];
+        if ((p.ld_v & 3) == 0) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float4 f = (live && 4 * c < rn) ? *reinterpret_cast<const float4 *>(vrow + 4 * c)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                vv[4 * c] = f.x;
+                vv[4 * c + 1] = f.y;
+                vv[4 * c + 2] = f.z;
+                vv[4 * c + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) vv[j] = (live && j < rn) ? vrow[j] : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c * 8 >= kpad) break;
+            uint4 hi4, lo4;
+            __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(&hi4);
+            __nv_bfloat16 *lo = reinterpret_cast<__nv_bfloat16 *>(&lo4);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = c * 8 + e;
+                const float val = j < rn ? s * vv[j] : 0.f;     // ranks past rn hold zeros (float4 over-read)
+                hi[e] = __float2bfloat16_rn(val);
+                lo[e] = __float2bfloat16_rn(val - __bfloat162float(hi[e]));
+            }
+            *reinterpret_cast<uint4 *>(a2hi + swz128(ethr, c)) = hi4;
+            *reinterpret_cast<uint4 *>(a2lo + swz128(ethr, c)) = lo4;
         }
     }
+    // B2: warp w loads 8-column groups g = w, w + 4, ... of the ranks lane and
+    // lane + 32 (16-byte loads of page rows), then writes them transposed.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        if (j >= kpad) break;
+        const __nv_bfloat16 *prow = page_row<__nv_bfloat16>(p.pv, page[h]);
+        uint4 d[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int col = nb * BN + (w + 4 * q) * 8;
+            d[q] = (j < rn && col < p.N) ? *reinterpret_cast<const uint4 *>(prow + col) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int n0 = (w + 4 * q) * 8;
+            const __nv_bfloat16 *e8 = reinterpret_cast<const __nv_bfloat16 *>(&d[q]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                *reinterpret_cast<__nv_bfloat16 *>(b2 + swz128(n0 + e, j >> 3) + (j & 7) * 2) = e8[e];
+        }
+    }
+    return rounds;
 }
 
-__device__ __forceinline__ void give_up(Ctrl *c, int *status) {
+template <int ST>
+__device__ __forceinline__ void give_up(Ctrl<ST> *c, int *status) {
     c->abort = 1;
     __threadfence_block();
     flag(status, LORA_DEV_WAIT_TIMEOUT);
 }
 
+template <int STAGES, bool FUSE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     layer_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                          LayerTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *a2hi = smem + STAGES * STAGE_BYTES;          // used when FUSE
+    uint8_t *a2lo = a2hi + A2_BYTES;
+    uint8_t *b2 = a2lo + A2_BYTES;
+    Ctrl<STAGES> *ctrl = reinterpret_cast<Ctrl<STAGES> *>(smem + STAGES * STAGE_BYTES + (FUSE ? 2 * A2_BYTES + B2_BYTES : 0));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = &ctrl->abort;
 
@@ -98,7 +203,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_init(&ctrl->tempty[b], 4);
         }
         mbar_init(&ctrl->drain, 1);
+        mbar_init(&ctrl->aready, 4);
+        mbar_init(&ctrl->aconsumed, 1);
         ctrl->abort = 0;
+        ctrl->akpad = 0;
+        ctrl->arounds = 0;
         mbar_fence_init();
         prefetch_tmap(&tmx);
         prefetch_tmap(&tmw);
@@ -152,6 +261,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
+            uint32_t n_ready = 0;          // aready phases consumed so far
             for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++local) {
                 const int b = local & 1;
                 const uint32_t u = (uint32_t)(local >> 1);
@@ -179,6 +289,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         phase ^= 1u;
                     }
                 }
+                if (ok && FUSE) {
+                    // the tile's low-rank term, 64 ranks per round:
+                    // acc += (s v)_hi . B + (s v)_lo . B over the round's ranks
+                    const uint32_t ah = smem_u32(a2hi), al = smem_u32(a2lo), bb = smem_u32(b2);
+                    int rounds = 1;
+                    for (int rd = 0; rd < rounds && ok; ++rd) {
+                        if (rd > 0) mma_commit(&ctrl->aconsumed);     // round rd-1's operands may be replaced
+                        if (!wait_phase(&ctrl->aready, n_ready++ & 1u, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after_sync();
+                        if (rd == 0) rounds = ctrl->arounds;
+                        const int kpad = ctrl->akpad;
+                        for (int kk = 0; kk < kpad / 16; ++kk) {
+                            mma_bf16(d, desc_kmajor_sw128(ah + kk * 32), desc_kmajor_sw128(bb + kk * 32), IDESC, 1);
+                            mma_bf16(d, desc_kmajor_sw128(al + kk * 32), desc_kmajor_sw128(bb + kk * 32), IDESC, 1);
+                        }
+                    }
+                    if (!ok) break;
+                }
                 if (ok) mma_commit(&ctrl->tfull[b]);
             }
             if (!ok) give_up(ctrl, p.status);
@@ -189,6 +320,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int sub = warp & 3;                      // TMEM sub-partition this warp may access
+        const int ethr = (warp - 2) * 32 + lane;       // 0..127
+        uint32_t n_consumed = 0;                       // aconsumed phases waited for so far
+        bool staged_ok = true;
+        // stage every round of a tile's adapter operands, handing each to the MMA warp
+        auto stage_tile = [&](int t) {
+            int rounds = 1;
+            for (int rd = 0; rd < rounds; ++rd) {
+                if (rd > 0) {
+                    const bool okc = wait_phase(&ctrl->aconsumed, n_consumed++ & 1u, abort);
+                    if (!__all_sync(0xffffffffu, okc)) {
+                        if (lane == 0) give_up(ctrl, p.status);
+                        staged_ok = false;
+                        return;
+                    }
+                }
+                rounds = fill_adapter<STAGES>(p, t, rd, a2hi, a2lo, b2, ctrl, ethr);
+                if (rounds < 1) rounds = 1;
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->aready);
+            }
+        };
+        if (FUSE && (int)blockIdx.x < p.num_tiles) stage_tile(blockIdx.x);
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int b = local & 1;
@@ -221,6 +375,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->tempty[b]);
+            // the tile's adapter MMAs are complete (tfull): stage the next tile's operands
+            if (FUSE && staged_ok && tile + (int)gridDim.x < p.num_tiles) stage_tile(tile + gridDim.x);
         }
     }
 
@@ -268,6 +424,22 @@ int num_sms() {
     return n;
 }
 
+template <int ST, bool FUSE>
+int launch_gemm_variant(const CUtensorMap &tmx, const CUtensorMap &tmw, const LayerTcParams &p, cudaStream_t st) {
+    const size_t smem = (size_t)ST * STAGE_BYTES + (FUSE ? 2 * A2_BYTES + B2_BYTES : 0) + sizeof(Ctrl<ST>) + 1024;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(layer_gemm_tc_kernel<ST, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return LORA_ERR_CUDA;
+        configured = true;
+    }
+    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+    layer_gemm_tc_kernel<ST, FUSE><<<grid, kThreadsTC, smem, st>>>(tmx, tmw, p);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 
 bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T) {
@@ -276,7 +448,7 @@ bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T) {
 }
 
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
-                   cudaStream_t st) {
+                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v) {
     CUtensorMap tmx, tmw;
     if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM) || !make_tmap(&tmw, W, (uint64_t)h_in, (uint64_t)h_out, BN))
         return LORA_ERR_CUDA;
@@ -290,18 +462,13 @@ int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, co
     p.num_tiles = p.num_m * p.num_n;
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.status = pool->d_status;
-    const size_t smem = (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(layer_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = true;
-    }
-    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-    layer_gemm_tc_kernel<<<grid, kThreadsTC, smem, st>>>(tmx, tmw, p);
-    count_launch();
-    return cuda_status(cudaGetLastError());
+    p.tile_ad = tile_ad;
+    p.pv = pool->view();
+    p.m = matrix;
+    p.v = v;
+    p.ld_v = ld_v;
+    if (tile_ad) return launch_gemm_variant<3, true>(tmx, tmw, p, st);
+    return launch_gemm_variant<4, false>(tmx, tmw, p, st);
 }
 
 }  // namespace lora

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) shrink_token_kernel(PoolView pv, int
                                                                 const int *__restrict__ seg_adapter, int S, int T) {
     extern __shared__ float vs[];
     const int t = blockIdx.x;
-    if (t == 0 && threadIdx.x == 0) check_segments(seg_starts, S, T, pv.status);
+    if (t == 0) check_segments(seg_starts, S, T, pv.status);
     const int a = seg_adapter[segment_of(seg_starts, S, t)];
     if (a < 0) return;
     const int *rec = lookup(pv, a, m);
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) expand_token_kernel(PoolView pv, int
                                                                 const int *__restrict__ seg_adapter, int S, int T) {
     extern __shared__ float vs[];
     const int t = blockIdx.x;
-    if (t == 0 && threadIdx.x == 0) check_segments(seg_starts, S, T, pv.status);
+    if (t == 0) check_segments(seg_starts, S, T, pv.status);
     const int a = seg_adapter[segment_of(seg_starts, S, t)];
     if (a < 0) return;
     const int *rec = lookup(pv, a, m);

@@ -67,7 +67,8 @@ extern "C" int lora_layer_forward_noalloc(lora_pool *p, int matrix, const void *
     if (T == 0) return LORA_OK;
     if (!x || !W || !y || !seg_starts || !seg_adapter || !aligned16(x) || !aligned16(W) || !aligned16(y))
         return LORA_ERR_ARG;
-    if ((size_t)T * (size_t)p->max_rank > kScratchFloats) return LORA_ERR_ARG;   // beyond the fixed scratch
+    if (lora_layer_forward_workspace_size(p, matrix, S, T) > LORA_NOALLOC_SCRATCH_BYTES)
+        return LORA_ERR_ARG;   // beyond the fixed scratch
     int device = -1;
     if (cudaGetDevice(&device) != cudaSuccess) {
         cudaGetLastError();

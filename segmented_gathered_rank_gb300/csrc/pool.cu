@@ -61,18 +61,27 @@ namespace lora {
 // low-rank term: shrink into v, expand into y.
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st) {
-    int rc = gemm_tc_ok(p, h_in, h_out, T) ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st)
-                                           : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
-    if (rc) return rc;
+    int rc;
+    const bool tc = gemm_tc_ok(p, h_in, h_out, T);
     if (sgmv_plan_ok(p, matrix, S) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
-        // tokens grouped by adapter (plan in the workspace, after v), then shrink and expand per group
+        // 1. plan: tokens grouped by adapter; GEMM tiles whose rows share one adapter
+        // 2. shrink v for every adapted token
+        // 3. base product; uniform tiles add their low-rank term inside the GEMM
+        // 4. expand the remaining rows
         int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
                                             ~uintptr_t(255));
-        if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st))) return rc;
+        int *tile_ad = tc ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
+        if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, tile_ad))) return rc;
         if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st)))
             return rc;
-        return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st);
+        rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank)
+                : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+        if (rc) return rc;
+        return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st,
+                                  tile_ad);
     }
+    rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st) : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+    if (rc) return rc;
     if ((rc = launch_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, st))) return rc;
     return launch_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, st);
 }

@@ -34,6 +34,7 @@ constexpr int kBlocksPerUnit = 4; // column blocks per expand unit (512 columns)
 constexpr int kStagesE = 3;
 constexpr int kMaxS = 8192;       // segments the segment-mode kernels take
 constexpr int kPlanThreads = 1024;
+constexpr int kTileRows = kFuseTileRows;   // M-tile rows of the tensor-core GEMM
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -196,6 +197,10 @@ struct PlanParams {
     int *status;
     int *plan;          // output, see ItemSource
     int max_items;
+    PoolView pv;        // for ranks of the tile classification
+    int m;
+    int *tile_ad;       // nullptr, or [n_tiles]: adapter whose term the GEMM adds for that M-tile, -1 if none
+    int n_tiles;
 };
 
 __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     int *wtot = sa + p.S;                // [kPlanThreads / 32 + 1]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = kPlanThreads / 32;
-    if (tid == 0) check_segments(p.seg_starts, p.S, p.T, p.status);
+    check_segments(p.seg_starts, p.S, p.T, p.status);
     for (int i = tid; i < p.n_ids; i += kPlanThreads) cnt[i] = 0;
     for (int s = tid; s <= p.S; s += kPlanThreads) sb[s] = min(max(p.seg_starts[s], 0), p.T);
     for (int s = tid; s < p.S; s += kPlanThreads) {
@@ -258,13 +263,60 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         for (int i = lane; i < n; i += 32)
             if (dst + i < p.T) perm[dst + i] = sb[s] + i;
     }
+    if (!p.tile_ad) return;
+    // GEMM M-tiles whose rows all use one adapter of rank 1..kFuseMaxRank: the
+    // GEMM adds that adapter's term itself, and the expand skips those rows.
+    // The flags are also kept in shared memory (in the counters' space, free
+    // by now) when they fit there.
+    __syncthreads();
+    int *tflag = cnt;
+    const bool staged = p.n_tiles <= 3 * p.n_ids + p.S;
+    for (int mb = tid; mb < p.n_tiles; mb += kPlanThreads) {
+        const int r0 = mb * kTileRows, r1 = min(p.T, r0 + kTileRows);
+        int lo = 0, hi = p.S;                   // first segment bound above r0
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sb[mid] > r0) hi = mid; else lo = mid + 1;
+        }
+        int a = -2;
+        bool uniform = true;
+        for (int s = max(lo - 1, 0); s < p.S && sb[s] < r1 && uniform; ++s) {
+            if (sb[s + 1] <= sb[s]) continue;
+            if (a == -2) a = sa[s];
+            else if (sa[s] != a) uniform = false;
+        }
+        int out = -1;
+        if (uniform && a >= 0 && a < p.pv.max_adapters) {
+            const int rank = p.pv.table[((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints];
+            if (rank >= 1 && rank <= kFuseMaxRank) out = a;
+        }
+        p.tile_ad[mb] = out;
+        if (staged) tflag[mb] = out;
+    }
+    __syncthreads();
+    // items all of whose rows sit in such tiles need no expand (the item's
+    // perm entries are read with independent loads)
+    for (int i = tid; i < min(n_items, p.max_items); i += kPlanThreads) {
+        const Item it = items[i];
+        if (it.a < 0) continue;
+        int tk[kM];
+#pragma unroll
+        for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? perm[it.off + k] : -1;
+        bool all = true;
+#pragma unroll
+        for (int k = 0; k < kM; ++k)
+            if (tk[k] >= 0) all &= (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0;
+        if (all) items[i].pad = 1;
+    }
 }
 
 // ---------------------------------------------------------------------------
-// Shrink: 128 threads, 32 tokens x (ranks) per item, K in 128-wide stages.
-// warp w: rows 16*(w & 1) .. +16, k half (w >> 1) of each stage.
+// Shrink: 128 threads, one half (16 tokens, grid.z) of an item x one chunk of
+// npc ranks (grid.y); K in 128-wide stages, warp w takes k 32w .. 32w+31 of
+// every stage and the four partial sums are added at the end.
 // ---------------------------------------------------------------------------
 constexpr int kThreadsS = 128;
+constexpr int kRowsS = 16;
 
 struct ShrinkParams {
     PoolView pv;
@@ -281,119 +333,135 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int pitch = kKs + 8;                                        // bf16 per smem row
     const int npc = p.npc;
-    __nv_bfloat16 *sx = reinterpret_cast<__nv_bfloat16 *>(smem_raw);     // [stages][kM][pitch]
-    __nv_bfloat16 *sa = sx + kStagesS * kM * pitch;                      // [stages][npc][pitch]
-    float *red = reinterpret_cast<float *>(sa + kStagesS * npc * pitch);  // [2][16][npc]
-    int *tok = reinterpret_cast<int *>(red + 2 * 16 * npc);              // [kM]
-    int *wtot = tok + kM;                                                // [8]
+    __nv_bfloat16 *sx = reinterpret_cast<__nv_bfloat16 *>(smem_raw);     // [stages][16][pitch]
+    __nv_bfloat16 *sa = sx + kStagesS * kRowsS * pitch;                  // [stages][npc][pitch]
+    float *red = reinterpret_cast<float *>(sa + kStagesS * npc * pitch);  // [3][16][npc] partials of warps 1..3
+    int *tok = reinterpret_cast<int *>(red + 3 * 16 * npc);              // [16]
+    int *wtot = tok + kRowsS;                                            // [8]
     int *rec = wtot + 8;                                                 // [rec_ints]
     int *scan = rec + p.pv.rec_ints;                                     // [S + 1]
 
-    if (blockIdx.x == 0 && tid == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
     const Item it = get_item<kThreadsS>(p.src, blockIdx.x, scan, wtot);
-    if (it.a < 0 || it.nt <= 0) return;
-    if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0)) return;
-    if ((int)blockIdx.y * p.npc >= min(rec[0], min(p.pv.max_rank, p.ld_v))) return;
-    if (tid < kM)
-        tok[tid] = tid < it.nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
-                               : 0;
+    const int row0 = blockIdx.z * kRowsS;
+    const int nt = min(kRowsS, it.nt - row0);
+    if (it.a < 0 || nt <= 0) return;
+    if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0 && blockIdx.z == 0)) return;
+    const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
+    const int j0 = blockIdx.y * npc;
+    if (j0 >= r) return;
+    const int np = min(npc, r - j0);
+    const int npad = (np + 15) & ~15;
+    if (tid < kRowsS)
+        tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + row0 + tid] : it.off + row0 + tid, 0),
+                                  p.src.T - 1)
+                            : 0;
+    // rows that never receive copies stay zero
+    for (int i = tid; i < kStagesS * kRowsS * (pitch / 8); i += kThreadsS)
+        if ((i / (pitch / 8)) % kRowsS >= nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < kStagesS * npc * (pitch / 8); i += kThreadsS)
+        if ((i / (pitch / 8)) % npc >= np) reinterpret_cast<uint4 *>(sa)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
-    const int mg = warp & 1, kh = warp >> 1;
     const int g = lane >> 2, q = lane & 3;
     const int nk = p.h_in / kKs;
-
-    // this CTA's ranks: chunk blockIdx.y of npc (ranks above an adapter's own are not its work)
-    for (int j0 = blockIdx.y * npc; j0 < min(r, (int)(blockIdx.y + 1) * npc); j0 += npc) {
-        const int np = min(npc, r - j0);
-        const int npad = (np + 15) & ~15;
-        // rows that never receive copies stay zero for the whole pass
-        for (int i = tid; i < kStagesS * kM * (pitch / 8); i += kThreadsS)
-            if ((i / (pitch / 8)) % kM >= it.nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < kStagesS * npc * (pitch / 8); i += kThreadsS)
-            if ((i / (pitch / 8)) % npc >= np) reinterpret_cast<uint4 *>(sa)[i] = make_uint4(0, 0, 0, 0);
-        auto issue = [&](int kc) {
-            const int st = kc % kStagesS;
-            __nv_bfloat16 *dx = sx + st * kM * pitch;
-            __nv_bfloat16 *da = sa + st * npc * pitch;
-            for (int i = tid; i < it.nt * (kKs / 8); i += kThreadsS) {
-                const int row = i >> 4, kv = i & 15;
-                cp_async16(dx + row * pitch + kv * 8, p.x + (long long)tok[row] * p.h_in + kc * kKs + kv * 8);
-            }
-            for (int i = tid; i < np * (kKs / 8); i += kThreadsS) {
-                const int row = i >> 4, kv = i & 15;
-                const int page = clamp_page(p.pv, rec[kRecHeader + j0 + row]);
-                cp_async16(da + row * pitch + kv * 8, page_row<__nv_bfloat16>(p.pv, page) + kc * kKs + kv * 8);
-            }
-        };
-        float d[8][4];
+    // this thread's 16-byte copy slots, fixed for the whole K loop: element
+    // tid + 128 k of the 16 rows x 16 chunks of x (k < 2) and of the npc rows
+    // x 16 chunks of A_T (k < 4)
+    const __nv_bfloat16 *xs[2], *as[4];
+    uint32_t xd[2], ad[4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * kThreadsS, row = i >> 4, kv = i & 15;
+        xs[k] = row < nt ? p.x + (long long)tok[row] * p.h_in + kv * 8 : nullptr;
+        xd[k] = (uint32_t)(row * pitch + kv * 8);
+    }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + k * kThreadsS, row = i >> 4, kv = i & 15;
+        as[k] = row < np ? page_row<__nv_bfloat16>(p.pv, clamp_page(p.pv, rec[kRecHeader + j0 + row])) + kv * 8 : nullptr;
+        ad[k] = (uint32_t)(row * pitch + kv * 8);
+    }
+    auto issue = [&](int kc) {
+        const int st = kc % kStagesS;
+        __nv_bfloat16 *dx = sx + st * kRowsS * pitch;
+        __nv_bfloat16 *da = sa + st * npc * pitch;
+        const int ko = kc * kKs;
 #pragma unroll
-        for (int kc = 0; kc < kStagesS - 1; ++kc) {
-            if (kc < nk) issue(kc);
-            cp_commit();
-        }
-        for (int kc = 0; kc < nk; ++kc) {
-            cp_wait<kStagesS - 2>();
-            __syncthreads();
-            if (kc + kStagesS - 1 < nk) issue(kc + kStagesS - 1);
-            cp_commit();
-            const int st = kc % kStagesS;
-            const __nv_bfloat16 *bx = sx + st * kM * pitch;
-            const __nv_bfloat16 *ba = sa + st * npc * pitch;
+        for (int k = 0; k < 2; ++k)
+            if (xs[k]) cp_async16(dx + xd[k], xs[k] + ko);
 #pragma unroll
-            for (int ks = 0; ks < kKs / 32; ++ks) {           // this warp's half of the stage
-                const int k = kh * (kKs / 2) + ks * 16;
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(bx + (mg * 16 + (lane & 15)) * pitch + k + (lane >> 4) * 8, a0, a1, a2, a3);
+        for (int k = 0; k < 4; ++k)
+            if (as[k]) cp_async16(da + ad[k], as[k] + ko);
+    };
+    float d[4][4];
 #pragma unroll
-                for (int t = 0; t < 8; t += 2) {
-                    if (t * 8 >= npad) break;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(ba + (t * 8 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k + ((lane >> 3) & 1) * 8, b0,
-                            b1, b2, b3);
-                    mma16816(d[t], a0, a1, a2, a3, b0, b1);
-                    mma16816(d[t + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-        }
-        cp_wait<0>();
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < kStagesS - 1; ++kc) {
+        if (kc < nk) issue(kc);
+        cp_commit();
+    }
+    for (int kc = 0; kc < nk; ++kc) {
+        cp_wait<kStagesS - 2>();
         __syncthreads();
-        // combine the two k halves and write v
-        float *rw = red + mg * 16 * npc;
-        if (kh == 1) {
+        if (kc + kStagesS - 1 < nk) issue(kc + kStagesS - 1);
+        cp_commit();
+        const int st = kc % kStagesS;
+        const __nv_bfloat16 *bx = sx + st * kRowsS * pitch;
+        const __nv_bfloat16 *ba = sa + st * npc * pitch;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
+        for (int ks = 0; ks < 2; ++ks) {                   // this warp's quarter of the stage
+            const int k = warp * 32 + ks * 16;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(bx + (lane & 15) * pitch + k + (lane >> 4) * 8, a0, a1, a2, a3);
+#pragma unroll
+            for (int t = 0; t < 4; t += 2) {
                 if (t * 8 >= npad) break;
-                rw[g * npc + t * 8 + 2 * q] = d[t][0];
-                rw[g * npc + t * 8 + 2 * q + 1] = d[t][1];
-                rw[(g + 8) * npc + t * 8 + 2 * q] = d[t][2];
-                rw[(g + 8) * npc + t * 8 + 2 * q + 1] = d[t][3];
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(ba + (t * 8 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k + ((lane >> 3) & 1) * 8, b0, b1,
+                        b2, b3);
+                mma16816(d[t], a0, a1, a2, a3, b0, b1);
+                mma16816(d[t + 1], a0, a1, a2, a3, b2, b3);
             }
         }
-        __syncthreads();
-        if (kh == 0) {
+    }
+    cp_wait<0>();
+    // add the four k-quarter partials and write v
+    if (warp > 0) {
+        float *rw = red + (warp - 1) * 16 * npc;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (t * 8 >= npad) break;
+        for (int t = 0; t < 4; ++t) {
+            if (t * 8 >= npad) break;
+            rw[g * npc + t * 8 + 2 * q] = d[t][0];
+            rw[g * npc + t * 8 + 2 * q + 1] = d[t][1];
+            rw[(g + 8) * npc + t * 8 + 2 * q] = d[t][2];
+            rw[(g + 8) * npc + t * 8 + 2 * q + 1] = d[t][3];
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int row = mg * 16 + g + 8 * h;
-                    const int j = t * 8 + 2 * q;
-                    if (row >= it.nt) continue;
-                    float *vrow = p.v + (long long)tok[row] * p.ld_v + j0;
-                    const float v0 = d[t][2 * h] + rw[(g + 8 * h) * npc + j];
-                    const float v1 = d[t][2 * h + 1] + rw[(g + 8 * h) * npc + j + 1];
-                    if (j < np) vrow[j] = v0;
-                    if (j + 1 < np) vrow[j + 1] = v1;
+        for (int t = 0; t < 4; ++t) {
+            if (t * 8 >= npad) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = g + 8 * h;
+                const int j = t * 8 + 2 * q;
+                if (row >= nt) continue;
+                float v0 = d[t][2 * h], v1 = d[t][2 * h + 1];
+#pragma unroll
+                for (int w = 0; w < 3; ++w) {
+                    v0 += red[w * 16 * npc + row * npc + j];
+                    v1 += red[w * 16 * npc + row * npc + j + 1];
                 }
+                float *vrow = p.v + (long long)tok[row] * p.ld_v + j0;
+                if (j < np) vrow[j] = v0;
+                if (j + 1 < np) vrow[j + 1] = v1;
             }
         }
-        __syncthreads();
     }
 }
 
@@ -414,6 +482,7 @@ struct ExpandParams {
     int ld_v;
     __nv_bfloat16 *y;
     int ncg;       // column groups per item
+    const int *tile_ad;   // nullptr, or per GEMM M-tile: >= 0 when the GEMM already added the term
 };
 
 __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams p) {
@@ -430,15 +499,24 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     int *rec = wtot + 8;
     int *scan = rec + p.pv.rec_ints;
 
-    if (blockIdx.x == 0 && tid == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
     const int cg = blockIdx.x % p.ncg;
     const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
     if (it.a < 0 || it.nt <= 0) return;
+    if (p.tile_ad && p.src.plan && it.pad) return;     // the GEMM added every row's term
     if (!load_record<kThreadsE>(p.pv, it.a, p.m, rec, tid == 0 && cg == 0)) return;
-    if (tid < kM)
-        tok[tid] = tid < it.nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
-                               : 0;
+    if (tid == 0) {   // the item's tokens, minus rows whose term the GEMM already added
+        int n = 0;
+        for (int k = 0; k < it.nt; ++k) {
+            const int t = min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + k] : it.off + k, 0), p.src.T - 1);
+            if (!p.tile_ad || p.tile_ad[t / kTileRows] < 0) tok[n++] = t;
+        }
+        for (int k = n; k < kM; ++k) tok[k] = 0;
+        wtot[0] = n;
+    }
     __syncthreads();
+    const int nt = wtot[0];
+    if (nt == 0) return;
     const int r_rec = min(rec[0], p.pv.max_rank);
     const int r = min(r_rec, p.ld_v);
     const float scale = __int_as_float(rec[1]);
@@ -453,26 +531,46 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     for (int j0 = 0; j0 < r; j0 += kpc) {
         const int rn = min(kpc, r - j0);
         const int kpad = (rn + 15) & ~15;
+        // this thread's 16-byte copy slots for the pass (fixed across column blocks):
+        // element tid + 128 k of the 32 rows x 16 chunks of y (k < 4) and of the
+        // kpc rows x 16 chunks of B (k < 8)
+        const __nv_bfloat16 *ysrc[4], *bsrc[8];
+        uint32_t ydst[4], bdst[8];
+        int ycv[4], bcv[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + k * kThreadsE, row = i >> 4, cv = i & 15;
+            ysrc[k] = row < nt ? p.y + (long long)tok[row] * p.h_out + cv * 8 : nullptr;
+            ydst[k] = (uint32_t)(row * yp + cv * 8);
+            ycv[k] = cv;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * kThreadsE, row = i >> 4, cv = i & 15;
+            bsrc[k] = row < rn ? page_row<__nv_bfloat16>(p.pv, clamp_page(p.pv, rec[kRecHeader + r_rec + j0 + row])) +
+                                     cv * 8
+                               : nullptr;
+            bdst[k] = (uint32_t)(row * yp + cv * 8);
+            bcv[k] = cv;
+        }
+        // B rows rn .. kpad-1 (MMA K padding) get no copies in this pass: zero them in every stage
+        for (int i = tid; i < kStagesE * (kpad - rn) * (kNb / 8); i += kThreadsE) {
+            const int st = i / ((kpad - rn) * (kNb / 8)), rem = i % ((kpad - rn) * (kNb / 8));
+            *reinterpret_cast<uint4 *>(sb + st * kpc * yp + (rn + (rem >> 4)) * yp + (rem & 15) * 8) =
+                make_uint4(0, 0, 0, 0);
+        }
         auto issue = [&](int bi) {
             const int st = bi % kStagesE;
             const int n0 = (b_first + bi) * kNb;
             const int ncv = min(kNb, p.h_out - n0) / 8;
             __nv_bfloat16 *dy = sy + st * kM * yp;
             __nv_bfloat16 *db = sb + st * kpc * yp;
-            for (int i = tid; i < it.nt * (kNb / 8); i += kThreadsE) {
-                const int row = i >> 4, cv = i & 15;
-                if (cv < ncv) cp_async16(dy + row * yp + cv * 8, p.y + (long long)tok[row] * p.h_out + n0 + cv * 8);
-            }
-            for (int i = tid; i < kpad * (kNb / 8); i += kThreadsE) {
-                const int row = i >> 4, cv = i & 15;
-                __nv_bfloat16 *dst = db + row * yp + cv * 8;
-                if (row < rn && cv < ncv) {
-                    const int page = clamp_page(p.pv, rec[kRecHeader + r_rec + j0 + row]);
-                    cp_async16(dst, page_row<__nv_bfloat16>(p.pv, page) + n0 + cv * 8);
-                } else {
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-                }
-            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (ysrc[k] && ycv[k] < ncv) cp_async16(dy + ydst[k], ysrc[k] + n0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (bsrc[k] && bcv[k] < ncv) cp_async16(db + bdst[k], bsrc[k] + n0);
         };
 #pragma unroll
         for (int bi = 0; bi < kStagesE - 1; ++bi) {
@@ -483,7 +581,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
         for (int i = tid; i < kM * kpad; i += kThreadsE) {
             const int row = i / kpad, j = i % kpad;
             float val = 0.f;
-            if (row < it.nt && j < rn) val = scale * p.v[(long long)tok[row] * p.ld_v + j0 + j];
+            if (row < nt && j < rn) val = scale * p.v[(long long)tok[row] * p.ld_v + j0 + j];
             const __nv_bfloat16 hi = __float2bfloat16_rn(val);
             svh[row * vp + j] = hi;
             svl[row * vp + j] = __float2bfloat16_rn(val - __bfloat162float(hi));
@@ -531,7 +629,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
             __syncthreads();
             const int n0 = (b_first + bi) * kNb;
             const int ncv = min(kNb, p.h_out - n0) / 8;
-            for (int i = tid; i < it.nt * (kNb / 8); i += kThreadsE) {
+            for (int i = tid; i < nt * (kNb / 8); i += kThreadsE) {
                 const int row = i >> 4, cv = i & 15;
                 if (cv < ncv)
                     *reinterpret_cast<uint4 *>(p.y + (long long)tok[row] * p.h_out + n0 + cv * 8) =
@@ -559,7 +657,13 @@ bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S) {
 
 size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T) {
     const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
-    return (size_t)(4 + ((T + 3) & ~3)) * 4 + (size_t)item_bound(n_ids, T) * sizeof(Item) + 64;
+    return (size_t)(4 + ((T + 3) & ~3)) * 4 + (size_t)item_bound(n_ids, T) * sizeof(Item) +
+           (size_t)((T + kTileRows - 1) / kTileRows) * 4 + 64;
+}
+
+int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan) {
+    const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
+    return plan + 4 + ((T + 3) & ~3) + item_bound(n_ids, T) * (int)(sizeof(Item) / sizeof(int));
 }
 
 bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S) {
@@ -568,7 +672,7 @@ bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S) {
 }
 
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                     int *plan, cudaStream_t st) {
+                     int *plan, cudaStream_t st, int *tile_ad) {
     PlanParams p;
     p.seg_starts = seg_starts;
     p.seg_adapter = seg_adapter;
@@ -578,6 +682,10 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.status = pool->d_status;
     p.plan = plan;
     p.max_items = item_bound(p.n_ids, T);
+    p.pv = pool->view();
+    p.m = matrix;
+    p.tile_ad = tile_ad;
+    p.n_tiles = (T + kTileRows - 1) / kTileRows;
     const size_t smem = (size_t)(3 * p.n_ids + 3 * S + 1 + kPlanThreads / 32 + 2) * 4;
     static size_t configured = 0;
     if (smem > configured) {
@@ -603,8 +711,8 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.v = v;
     p.ld_v = ld_v;
-    const size_t smem = (size_t)kStagesS * (kM + p.npc) * (kKs + 8) * 2 + (size_t)2 * 16 * p.npc * 4 +
-                        (size_t)(kM + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
+    const size_t smem = (size_t)kStagesS * (kRowsS + p.npc) * (kKs + 8) * 2 + (size_t)3 * 16 * p.npc * 4 +
+                        (size_t)(kRowsS + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
     static size_t configured = 0;
     if (smem > configured) {
         if (cudaFuncSetAttribute(sgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -613,7 +721,7 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
         configured = smem;
     }
     const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
-    const dim3 grid(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc);
+    const dim3 grid(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc, kM / kRowsS);
     sgmv_shrink_kernel<<<grid, kThreadsS, smem, st>>>(p);
     count_launch();
     return cuda_status(cudaGetLastError());
@@ -621,7 +729,7 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
 
 int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
-                       cudaStream_t st) {
+                       cudaStream_t st, const int *tile_ad) {
     ExpandParams p;
     p.pv = pool->view();
     p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
@@ -631,6 +739,7 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
     p.v = v;
     p.ld_v = ld_v;
     p.y = static_cast<__nv_bfloat16 *>(y);
+    p.tile_ad = tile_ad;
     const int nb_total = (h_out + kNb - 1) / kNb;
     p.ncg = (nb_total + kBlocksPerUnit - 1) / kBlocksPerUnit;
     const size_t smem = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
