@@ -113,9 +113,10 @@ int lora_pool_destroy(lora_pool *pool);
  *   B    rank x h_out (row-major, pool dtype).
  * The first load on a matrix fixes that matrix's (h_in, h_out); later loads
  * must match (else LORA_ERR_SHAPE).  A previous adapter in the same entry is
- * replaced.  The host arrays are copied before the call returns (they may be
- * freed at once); the device copy and the table update are enqueued on
- * `stream`: work that uses the adapter must be ordered after them.
+ * replaced.  The device copy and the table update run on `stream` (after the
+ * work already queued there) and the call returns once they are complete:
+ * the adapter is resident for every kernel launched afterwards, on any
+ * stream, and the host arrays may be freed at once.
  * rank == 0 is legal (the adapter adds nothing).
  * Errors: LORA_ERR_ARG, LORA_ERR_RANK, LORA_ERR_SHAPE, LORA_ERR_POOL_FULL
  * (the pool is unchanged), LORA_ERR_CUDA.
@@ -192,8 +193,9 @@ int lora_layer_forward(lora_pool *pool, int matrix, const void *x, const void *W
  * LORA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library keeps until the process exits.  Requires
  * lora_layer_forward_workspace_size(pool, matrix, S, T) <=
- * LORA_NOALLOC_SCRATCH_BYTES (about T * max_rank * 4 bytes plus a small
- * per-token plan; else LORA_ERR_ARG) and the pool's device to be current
+ * LORA_NOALLOC_SCRATCH_BYTES (about 5 * T * max_rank * 4 bytes -- v and the
+ * tensor-core shrink's four K-split partials -- plus a small per-token plan;
+ * else LORA_ERR_ARG) and the pool's device to be current
  * (else LORA_ERR_ARG).  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress); make
  * that first call before any stream capture.  All calls share the array:
@@ -201,7 +203,7 @@ int lora_layer_forward(lora_pool *pool, int matrix, const void *x, const void *W
  * caller.  Allocates nothing (no cudaMalloc/cudaFree or allocating library
  * routine).
  */
-#define LORA_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+#define LORA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int lora_layer_forward_noalloc(lora_pool *pool, int matrix, const void *x, const void *W, void *y,
                                const int *seg_starts, const int *seg_adapter, int S, int T,
                                lora_stream stream);

@@ -77,7 +77,6 @@ struct lora_pool {
     void *d_stage;
     size_t stage_bytes;
     cudaEvent_t stage_done;
-    bool stage_pending;
 
     lora::PoolView view() const {
         lora::PoolView v;
@@ -206,9 +205,11 @@ int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, 
 bool sgmv_shrink_ok(const lora_pool *pool, int h_in, int S);
 bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S);
 // plan: nullptr (items from the segment table) or a plan from launch_sgmv_plan
+// skip_fused: the plan's item masks name rows whose v the tensor-core shrink computes; items
+// all of whose rows are such rows are skipped.
 int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
-                       cudaStream_t st);
+                       cudaStream_t st, bool skip_fused = false);
 int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
                        cudaStream_t st, const int *tile_ad = nullptr);
@@ -220,12 +221,20 @@ int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan);
 // tile_ad != nullptr: also classify the GEMM's 128-row M-tiles (see launch_gemm_tc).
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
                      int *plan, cudaStream_t st, int *tile_ad = nullptr);
+int num_sms();   // SMs of the current device (cached)
 bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
 // tile_ad != nullptr: M-tiles with tile_ad[m] >= 0 also get that adapter's term
-// s * v . B (v: T x ld_v fp32 from the shrink) inside the GEMM.
+// s * v . B inside the GEMM, v being the sum of the nsplit partials
+// v[s][T][ld_v] that launch_shrink_tc wrote.
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
                    cudaStream_t st, int matrix = 0, const int *tile_ad = nullptr, const float *v = nullptr,
-                   int ld_v = 0);
+                   int ld_v = 0, int nsplit = 1);
+// K splits of the tensor-core shrink (at most kShrinkTcSplits).
+constexpr int kShrinkTcSplits = 4;
+int shrink_tc_splits(int h_in);
+// v partials [shrink_tc_splits(h_in)][T][ld_v] of the M-tiles with tile_ad[m] >= 0.
+int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, const int *tile_ad,
+                     float *vpart, int ld_v, cudaStream_t st);
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st);
 int launch_base_gemm(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y,

@@ -21,6 +21,8 @@
 // for its own copies and MMAs in flight, and the CTA frees its TMEM.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "internal.cuh"
 #include "tc_common.cuh"
 
@@ -49,8 +51,10 @@ struct LayerTcParams {
     const int *tile_ad;     // per M-tile: adapter whose term is added here, or -1
     PoolView pv;
     int m;
-    const float *v;
+    const float *v;         // [nsplit][T][ld_v]: K-split partial sums of x . A_a for the fused tiles' rows
     int ld_v;
+    int nsplit;
+    long long split_stride; // floats between partials
 };
 
 template <int ST>
@@ -116,31 +120,38 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
         const int row = mb * BM + ethr;
         const bool live = row < p.T;
         const float *vrow = p.v + (long long)(live ? row : 0) * p.ld_v + j0;
-        float vv[64];
-        if ((p.ld_v & 3) == 0) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 f = (live && 4 * c < rn) ? *reinterpret_cast<const float4 *>(vrow + 4 * c)
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                vv[4 * c] = f.x;
-                vv[4 * c + 1] = f.y;
-                vv[4 * c + 2] = f.z;
-                vv[4 * c + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) vv[j] = (live && j < rn) ? vrow[j] : 0.f;
-        }
+        const bool vec = (p.ld_v & 3) == 0;
+        // 8 ranks at a time: the K-split partials added in a fixed order (deterministic)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             if (c * 8 >= kpad) break;
+            float vv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vv[e] = 0.f;
+            const float *vp = vrow + c * 8;
+            for (int sp = 0; sp < p.nsplit; ++sp, vp += p.split_stride) {
+                if (vec) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float4 f = (live && c * 8 + 4 * h < rn) ? *reinterpret_cast<const float4 *>(vp + 4 * h)
+                                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                        vv[4 * h] += f.x;
+                        vv[4 * h + 1] += f.y;
+                        vv[4 * h + 2] += f.z;
+                        vv[4 * h + 3] += f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vv[e] += (live && c * 8 + e < rn) ? vp[e] : 0.f;
+                }
+            }
             uint4 hi4, lo4;
             __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(&hi4);
             __nv_bfloat16 *lo = reinterpret_cast<__nv_bfloat16 *>(&lo4);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int j = c * 8 + e;
-                const float val = j < rn ? s * vv[j] : 0.f;     // ranks past rn hold zeros (float4 over-read)
+                const float val = j < rn ? s * vv[e] : 0.f;     // ranks past rn hold zeros (float4 over-read)
                 hi[e] = __float2bfloat16_rn(val);
                 lo[e] = __float2bfloat16_rn(val - __bfloat162float(hi[e]));
             }
@@ -386,6 +397,200 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Shrink of the fused M-tiles on the tensor cores.  For an M-tile whose 128
+// rows all use adapter a (rank r <= kFuseMaxRank) the shrink is a dense
+// contraction v = x[tile] . A_a^T with M = 128, N = r, K = h_in; at rank 128
+// that is 256 flops per x element, more than warp-level MMAs sustain at HBM
+// rate.  Grid (M-tiles, K splits); a CTA whose tile is not fused exits at
+// once.  Through a 6-stage ring, warp 0 streams x (one 128 x 64 TMA box,
+// 128-byte swizzle) and warps 2-5 the r page rows of A_a (16-byte cp.async
+// into the same swizzled K-major layout, each thread's copies arriving on the
+// stage's mbarrier as they land); warp 1 issues tcgen05.mma (M 128, N = r
+// rounded up to 16) into TMEM; then warps 2-5 read the accumulator and store
+// the split's partial sums, which the GEMM adds in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int SK_STAGES = 6;
+constexpr int SK_X_BYTES = BM * BK * 2;
+constexpr int SK_A_BYTES = kFuseMaxRank * BK * 2;
+constexpr int SK_STAGE_BYTES = SK_X_BYTES + SK_A_BYTES;
+constexpr uint32_t SK_TMEM_COLS = kFuseMaxRank;
+
+struct ShrinkTcParams {
+    int T, num_k, nsplit;
+    const int *tile_ad;
+    PoolView pv;
+    int m;
+    float *vpart;           // [nsplit][T][ld_v]
+    int ld_v;
+    long long split_stride;
+    int *status;
+};
+
+struct SkCtrl {
+    uint64_t full[SK_STAGES];
+    uint64_t empty[SK_STAGES];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    int page[kFuseMaxRank];
+};
+
+__device__ __forceinline__ void cp_async16_sk(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival was counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_sk(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_wait_all_sk() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    shrink_tc_kernel(const __grid_constant__ CUtensorMap tmx, ShrinkTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SkCtrl *ctrl = reinterpret_cast<SkCtrl *>(smem + SK_STAGES * SK_STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mb = blockIdx.x, split = blockIdx.y;
+    const int a = p.tile_ad[mb];
+    if (a < 0 || a >= p.pv.max_adapters) return;
+    const int *rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
+    const int r = rec[0];
+    if (r < 1 || r > kFuseMaxRank || r > p.ld_v) return;     // the GEMM adds nothing for such a tile either
+    const int npad = (r + 15) & ~15;
+    const uint32_t idesc = idesc_bf16_f32(BM, npad);
+    const int kb0 = split * p.num_k / p.nsplit, kb1 = (split + 1) * p.num_k / p.nsplit;
+    volatile int *abort = &ctrl->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SK_STAGES; ++s) {
+            mbar_init(&ctrl->full[s], 129);    // the x TMA (with its bytes) + 128 threads' A copies
+            mbar_init(&ctrl->empty[s], 1);
+        }
+        mbar_init(&ctrl->done, 1);
+        ctrl->abort = 0;
+        mbar_fence_init();
+        prefetch_tmap(&tmx);
+    }
+    for (int j = threadIdx.x; j < r; j += kThreadsTC) {
+        const int pg = rec[kRecHeader + j];
+        ctrl->page[j] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctrl->tmem_base, SK_TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = ctrl->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ x producer (one lane)
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const int i = kb - kb0, stage = i % SK_STAGES;
+                const uint32_t phase = (uint32_t)(i / SK_STAGES) & 1u;
+                if (!wait_phase(&ctrl->empty[stage], phase ^ 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&ctrl->full[stage], (uint32_t)SK_X_BYTES);
+                tma_load_2d(smem + stage * SK_STAGE_BYTES, &tmx, kb * BK, mb * BM, &ctrl->full[stage]);
+                ++issued;
+            }
+            if (!ok) {
+                ctrl->abort = 1;
+                __threadfence_block();
+                flag(p.status, LORA_DEV_WAIT_TIMEOUT);
+                // the x copies still landing must land before exit (the A copies arrive by themselves)
+                for (int i = issued > SK_STAGES ? issued - SK_STAGES : 0; i < issued; ++i)
+                    wait_phase(&ctrl->full[i % SK_STAGES], (uint32_t)(i / SK_STAGES) & 1u, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const int i = kb - kb0, stage = i % SK_STAGES;
+                const uint32_t phase = (uint32_t)(i / SK_STAGES) & 1u;
+                if (!wait_phase(&ctrl->full[stage], phase, abort)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async();                  // the A rows came through the generic proxy
+                fence_after_sync();
+                const uint32_t a0 = smem_u32(smem + stage * SK_STAGE_BYTES);
+                const uint32_t b0 = a0 + SK_X_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    mma_bf16(tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), idesc,
+                             (i | k) != 0);
+                mma_commit(&ctrl->empty[stage]);
+            }
+            if (!ok) {
+                ctrl->abort = 1;
+                __threadfence_block();
+                flag(p.status, LORA_DEV_WAIT_TIMEOUT);
+            }
+            mma_commit(&ctrl->done);                 // every MMA of this CTA complete before TMEM is read or freed
+            wait_phase(&ctrl->done, 0, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ warps 2..5: A producers, then epilogue
+        // thread t: 16-byte chunk c = t & 7 of rank rows (t >> 3) + 16 q.  Each
+        // thread's copies of a stage arrive on the stage's barrier when they land.
+        const int t = threadIdx.x - 64, c = t & 7;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            const int i = kb - kb0, stage = i % SK_STAGES;
+            const uint32_t phase = (uint32_t)(i / SK_STAGES) & 1u;
+            if (!wait_phase(&ctrl->empty[stage], phase ^ 1u, abort)) break;
+            const uint32_t sa = smem_u32(smem + stage * SK_STAGE_BYTES + SK_X_BYTES);
+            for (int j = t >> 3; j < r; j += 16)
+                cp_async16_sk(sa + swz128(j, c), page_row<__nv_bfloat16>(p.pv, ctrl->page[j]) + kb * BK + c * 8);
+            cp_async_arrive_sk(&ctrl->full[stage]);
+        }
+        cp_wait_all_sk();                            // nothing lands after the CTA exits
+
+        const int sub = warp & 3;
+        const bool ok = wait_phase(&ctrl->done, 0, nullptr) && !*abort;
+        if (__all_sync(0xffffffffu, ok)) {
+            fence_after_sync();
+            const int row = mb * BM + sub * 32 + lane;
+            float *out = p.vpart + (long long)split * p.split_stride + (long long)row * p.ld_v;
+            const bool vec = (p.ld_v & 3) == 0;
+            for (int c0 = 0; c0 < npad; c0 += 32) {
+                float f[32];
+                __syncwarp();
+                tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
+                if (row < p.T) {
+                    if (vec) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            if (c0 + e < r)   // r <= ld_v and ld_v % 4 == 0: the float4 stays in the row
+                                *reinterpret_cast<float4 *>(out + c0 + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c0 + e < r) out[c0 + e] = f[e];
+                    }
+                }
+            }
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, SK_TMEM_COLS);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -414,16 +619,6 @@ bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t oute
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int num_sms() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
-    }
-    return n;
-}
-
 template <int ST, bool FUSE>
 int launch_gemm_variant(const CUtensorMap &tmx, const CUtensorMap &tmw, const LayerTcParams &p, cudaStream_t st) {
     const size_t smem = (size_t)ST * STAGE_BYTES + (FUSE ? 2 * A2_BYTES + B2_BYTES : 0) + sizeof(Ctrl<ST>) + 1024;
@@ -448,7 +643,7 @@ bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T) {
 }
 
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
-                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v) {
+                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v, int nsplit) {
     CUtensorMap tmx, tmw;
     if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM) || !make_tmap(&tmw, W, (uint64_t)h_in, (uint64_t)h_out, BN))
         return LORA_ERR_CUDA;
@@ -467,8 +662,41 @@ int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, co
     p.m = matrix;
     p.v = v;
     p.ld_v = ld_v;
+    p.nsplit = nsplit;
+    p.split_stride = (long long)T * ld_v;
     if (tile_ad) return launch_gemm_variant<3, true>(tmx, tmw, p, st);
     return launch_gemm_variant<4, false>(tmx, tmw, p, st);
+}
+
+int shrink_tc_splits(int h_in) { return std::max(1, std::min(kShrinkTcSplits, h_in / BK)); }
+
+int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, const int *tile_ad,
+                     float *vpart, int ld_v, cudaStream_t st) {
+    CUtensorMap tmx;
+    if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM)) return LORA_ERR_CUDA;
+    ShrinkTcParams p;
+    p.T = T;
+    p.num_k = h_in / BK;
+    p.nsplit = shrink_tc_splits(h_in);
+    p.tile_ad = tile_ad;
+    p.pv = pool->view();
+    p.m = matrix;
+    p.vpart = vpart;
+    p.ld_v = ld_v;
+    p.split_stride = (long long)T * ld_v;
+    p.status = pool->d_status;
+    const size_t smem = (size_t)SK_STAGES * SK_STAGE_BYTES + sizeof(SkCtrl) + 1024;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(shrink_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        configured = true;
+    }
+    const dim3 grid((T + BM - 1) / BM, p.nsplit);
+    shrink_tc_kernel<<<grid, kThreadsTC, smem, st>>>(tmx, p);
+    count_launch();
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace lora

@@ -11,6 +11,17 @@
 #include "internal.cuh"
 
 namespace lora {
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+    }
+    return n;
+}
+
 std::atomic<unsigned long long> g_launches{0};
 
 // Copies one staged row per block into its page and (block 0) writes the
@@ -64,17 +75,23 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
     int rc;
     const bool tc = gemm_tc_ok(p, h_in, h_out, T);
     if (sgmv_plan_ok(p, matrix, S) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
-        // 1. plan: tokens grouped by adapter; GEMM tiles whose rows share one adapter
-        // 2. shrink v for every adapted token
-        // 3. base product; uniform tiles add their low-rank term inside the GEMM
-        // 4. expand the remaining rows
-        int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
-                                            ~uintptr_t(255));
+        // 1. plan: tokens grouped by adapter; GEMM M-tiles whose rows share one adapter
+        // 2. (tensor cores) v of those tiles: K-split partials of M 128 x N r contractions
+        // 3. v of every other adapted token (warp-MMA SGMV shrink)
+        // 4. base product; the uniform tiles add their low-rank term inside the GEMM
+        // 5. expand the remaining rows
+        const size_t vfloats = (size_t)T * p->max_rank;
+        float *vpart = v + vfloats;
+        int *plan = reinterpret_cast<int *>(
+            (reinterpret_cast<uintptr_t>(vpart + (size_t)kShrinkTcSplits * vfloats) + 255) & ~uintptr_t(255));
         int *tile_ad = tc ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
         if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, tile_ad))) return rc;
-        if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st)))
+        if (tc && (rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, vpart, p->max_rank, st))) return rc;
+        if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st,
+                                     tc)))
             return rc;
-        rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank)
+        rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, vpart, p->max_rank,
+                                 shrink_tc_splits(h_in))
                 : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
         if (rc) return rc;
         return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st,
@@ -128,7 +145,6 @@ int lora_pool_create(lora_pool **out, int dtype, int page_elems, int n_pages, in
     p->d_status = nullptr;
     p->h_stage = p->d_stage = nullptr;
     p->stage_done = nullptr;
-    p->stage_pending = false;
     const size_t n_rec = (size_t)max_adapters * n_matrices;
     p->stage_bytes = (size_t)2 * max_rank * page_elems * p->esize + 256 + sizeof(LoadArgs);
     int rc = LORA_OK;
@@ -207,11 +223,6 @@ int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale,
         if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
         release_pages(p, ri);
     }
-    // The staging buffers are reused: wait for the previous load's scatter.
-    if (p->stage_pending) {
-        if (cudaEventSynchronize(p->stage_done) != cudaSuccess) return LORA_ERR_CUDA;
-        p->stage_pending = false;
-    }
     const int rba = h_in * p->esize, rbb = h_out * p->esize;
     const size_t data_bytes = (size_t)rank * (rba + rbb);
     const size_t args_off = (data_bytes + 255) & ~(size_t)255;
@@ -245,7 +256,13 @@ int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale,
         for (int i = 2 * rank - 1; i >= 0; --i) p->free_pages.push_back(la->ids[i]);
         return LORA_ERR_CUDA;
     }
-    p->stage_pending = true;
+    // The call returns with the adapter resident: the BGMV kernel reads page
+    // tables and pages before it waits on the kernel ahead of it in its
+    // stream, so no load may still be in flight when a kernel is launched.
+    if (cudaEventSynchronize(p->stage_done) != cudaSuccess) {
+        for (int i = 2 * rank - 1; i >= 0; --i) p->free_pages.push_back(la->ids[i]);
+        return LORA_ERR_CUDA;
+    }
     hrec[0] = rank;
     std::memcpy(&hrec[1], &scale, sizeof(int));
     for (int i = 0; i < 2 * rank; ++i) hrec[kRecHeader + i] = la->ids[i];
@@ -328,7 +345,8 @@ int lora_bgmv(lora_pool *p, int matrix, const void *x, void *y, const int *token
 size_t lora_layer_forward_workspace_size(const lora_pool *p, int matrix, int S, int T) {
     int h_in, h_out;
     if (!p || T < 0 || S < 0 || matrix_dims(p, matrix, &h_in, &h_out)) return 0;
-    return (size_t)T * p->max_rank * sizeof(float) + sgmv_plan_bytes(p, matrix, T) + 256;
+    // v, the tensor-core shrink's K-split partials, then (256-byte aligned) the plan
+    return (size_t)T * p->max_rank * sizeof(float) * (1 + kShrinkTcSplits) + sgmv_plan_bytes(p, matrix, T) + 256;
 }
 
 int lora_layer_forward(lora_pool *p, int matrix, const void *x, const void *W, void *y,

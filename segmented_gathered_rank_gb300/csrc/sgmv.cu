@@ -26,7 +26,8 @@
 namespace lora {
 namespace {
 
-constexpr int kM = 32;            // tokens per item
+constexpr int kM = 32;            // tokens per item (one per lane where a warp collects an item's tokens)
+static_assert(kM == 32, "an item's tokens are collected one per lane of a warp");
 constexpr int kKs = 128;          // k per shrink pipeline stage
 constexpr int kStagesS = 4;
 constexpr int kNb = 128;          // output columns per expand block
@@ -113,7 +114,7 @@ struct Item {
     int a;
     int off;
     int nt;
-    int pad;
+    int pad;    // plan with GEMM-fused tiles: bit k set when row k's term is added by the GEMM
 };
 
 // Item `idx` among the (segment, kM-token chunk) pairs of a segment table.
@@ -153,7 +154,8 @@ __device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int 
 struct ItemSource {
     const int *seg_starts, *seg_adapter;
     int S, T;
-    const int *plan;     // nullptr, or [n_items, pad x3, perm[T], items[...] as Item]
+    const int *plan;     // nullptr, or [n_items, n_work, pad x2, perm[T], items[...] as Item, ...]
+    const Item *work;    // nullptr, or the plan's compacted items that still have rows to do (count plan[1])
 };
 
 __device__ __forceinline__ const int *plan_perm(const int *plan) { return plan + 4; }
@@ -163,10 +165,11 @@ __device__ __forceinline__ const Item *plan_items(const int *plan, int T) {
 
 template <int NT>
 __device__ Item get_item(const ItemSource &src, int idx, int *scan, int *wtot) {
-    if (src.plan) {
-        if (idx >= src.plan[0]) return Item{-1, 0, 0, 0};
-        return plan_items(src.plan, src.T)[idx];
+    if (src.work) {       // both loads at once; an index past the count reads an unused slot and drops it
+        const Item it = src.work[idx];
+        return idx < src.plan[1] ? it : Item{-1, 0, 0, 0};
     }
+    if (src.plan) return plan_items(src.plan, src.T)[idx];   // idx < the plan's item bound; unused items have a = -1
     return segment_item<NT>(src.seg_starts, src.seg_adapter, src.S, src.T, idx, scan, wtot);
 }
 
@@ -201,6 +204,7 @@ struct PlanParams {
     int m;
     int *tile_ad;       // nullptr, or [n_tiles]: adapter whose term the GEMM adds for that M-tile, -1 if none
     int n_tiles;
+    Item *work;         // with tile_ad: compacted copies of the items that keep rows outside such tiles
 };
 
 __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
@@ -248,6 +252,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         }
     }
     if (tid == 0) p.plan[0] = min(n_items, p.max_items);
+    for (int i = n_items + tid; i < p.max_items; i += kPlanThreads) items[i] = Item{-1, 0, 0, 0};
     // token permutation: short segments one per thread, long ones one per warp
     for (int s = tid; s < p.S; s += kPlanThreads) {
         const int n = sb[s + 1] - sb[s];
@@ -264,6 +269,8 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
             if (dst + i < p.T) perm[dst + i] = sb[s] + i;
     }
     if (!p.tile_ad) return;
+    int *wcount = wtot + nwarps + 1;        // past block_scan's words
+    if (tid == 0) *wcount = 0;
     // GEMM M-tiles whose rows all use one adapter of rank 1..kFuseMaxRank: the
     // GEMM adds that adapter's term itself, and the expand skips those rows.
     // The flags are also kept in shared memory (in the counters' space, free
@@ -294,20 +301,28 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         if (staged) tflag[mb] = out;
     }
     __syncthreads();
-    // items all of whose rows sit in such tiles need no expand (the item's
-    // perm entries are read with independent loads)
+    // each item's mask of rows that sit in such tiles (the expand skips them;
+    // the item's perm entries are read with independent loads)
     for (int i = tid; i < min(n_items, p.max_items); i += kPlanThreads) {
         const Item it = items[i];
         if (it.a < 0) continue;
         int tk[kM];
 #pragma unroll
         for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? perm[it.off + k] : -1;
-        bool all = true;
+        unsigned mask = 0;
 #pragma unroll
         for (int k = 0; k < kM; ++k)
-            if (tk[k] >= 0) all &= (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0;
-        if (all) items[i].pad = 1;
+            if (tk[k] >= 0 && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0) mask |= 1u << k;
+        items[i].pad = (int)mask;
+        const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
+        if ((mask & all) != all) {   // rows left for the SGMV kernels (slot order is immaterial)
+            Item w = it;
+            w.pad = (int)mask;
+            p.work[atomicAdd(wcount, 1)] = w;
+        }
     }
+    __syncthreads();
+    if (tid == 0) p.plan[1] = *wcount;
 }
 
 // ---------------------------------------------------------------------------
@@ -322,6 +337,7 @@ struct ShrinkParams {
     PoolView pv;
     ItemSource src;
     int m, h_in;
+    bool skip_fused;   // skip plan items whose rows all sit in tensor-core-shrunk tiles
     int npc;       // ranks per CTA: max_rank rounded up to 16, at most 32 (grid.y covers the rest)
     const __nv_bfloat16 *x;
     float *v;
@@ -346,6 +362,10 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
     const int row0 = blockIdx.z * kRowsS;
     const int nt = min(kRowsS, it.nt - row0);
     if (it.a < 0 || nt <= 0) return;
+    if (p.skip_fused && p.src.plan) {
+        const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
+        if (((unsigned)it.pad & all) == all) return;
+    }
     if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0 && blockIdx.z == 0)) return;
     const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
     const int j0 = blockIdx.y * npc;
@@ -482,7 +502,7 @@ struct ExpandParams {
     int ld_v;
     __nv_bfloat16 *y;
     int ncg;       // column groups per item
-    const int *tile_ad;   // nullptr, or per GEMM M-tile: >= 0 when the GEMM already added the term
+    const int *tile_ad;   // non-null: the plan's item masks name rows whose term the GEMM already added
 };
 
 __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams p) {
@@ -499,22 +519,36 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     int *rec = wtot + 8;
     int *scan = rec + p.pv.rec_ints;
 
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
     const int cg = blockIdx.x % p.ncg;
     const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
     if (it.a < 0 || it.nt <= 0) return;
-    if (p.tile_ad && p.src.plan && it.pad) return;     // the GEMM added every row's term
-    if (!load_record<kThreadsE>(p.pv, it.a, p.m, rec, tid == 0 && cg == 0)) return;
-    if (tid == 0) {   // the item's tokens, minus rows whose term the GEMM already added
-        int n = 0;
-        for (int k = 0; k < it.nt; ++k) {
-            const int t = min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + k] : it.off + k, 0), p.src.T - 1);
-            if (!p.tile_ad || p.tile_ad[t / kTileRows] < 0) tok[n++] = t;
-        }
-        for (int k = n; k < kM; ++k) tok[k] = 0;
-        wtot[0] = n;
+    const unsigned fused = (p.tile_ad && p.src.plan) ? (unsigned)it.pad : 0u;
+    const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
+    if ((fused & all) == all) return;            // the GEMM added every row's term
+    if (it.a >= p.pv.max_adapters) {
+        if (tid == 0 && cg == 0) flag(p.pv.status, LORA_DEV_BAD_ADAPTER);
+        return;
+    }
+    // the record and the item's tokens load together
+    for (int i = tid; i < p.pv.rec_ints; i += kThreadsE)
+        rec[i] = p.pv.table[((long long)it.a * p.pv.n_matrices + p.m) * p.pv.rec_ints + i];
+    if (warp == 0) {   // the item's tokens, minus rows whose term the GEMM already added (one per lane)
+        const bool keep = lane < it.nt && !((fused >> lane) & 1u);
+        const int t = keep ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + lane] : it.off + lane, 0),
+                                 p.src.T - 1)
+                           : 0;
+        const unsigned kept = __ballot_sync(0xffffffffu, keep);
+        const int n = __popc(kept);
+        if (keep) tok[__popc(kept & ((1u << lane) - 1u))] = t;
+        if (lane >= n) tok[lane] = 0;
+        if (lane == 0) wtot[0] = n;
     }
     __syncthreads();
+    if (rec[0] < 0) {
+        if (tid == 0 && cg == 0) flag(p.pv.status, LORA_DEV_BAD_ADAPTER);
+        return;
+    }
     const int nt = wtot[0];
     if (nt == 0) return;
     const int r_rec = min(rec[0], p.pv.max_rank);
@@ -657,8 +691,17 @@ bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S) {
 
 size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T) {
     const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
-    return (size_t)(4 + ((T + 3) & ~3)) * 4 + (size_t)item_bound(n_ids, T) * sizeof(Item) +
-           (size_t)((T + kTileRows - 1) / kTileRows) * 4 + 64;
+    const int n_tiles = (T + kTileRows - 1) / kTileRows;
+    return (size_t)(4 + ((T + 3) & ~3)) * 4 + (size_t)2 * item_bound(n_ids, T) * sizeof(Item) +
+           (size_t)((n_tiles + 3) & ~3) * 4 + 64;
+}
+
+// The plan's compacted work items (after its M-tile array, 16-byte aligned).
+static Item *sgmv_plan_work(const lora_pool *pool, int matrix, int T, int *plan) {
+    const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
+    const int n_tiles = (T + kTileRows - 1) / kTileRows;
+    return reinterpret_cast<Item *>(plan + 4 + ((T + 3) & ~3) + item_bound(n_ids, T) * (int)(sizeof(Item) / sizeof(int)) +
+                                    ((n_tiles + 3) & ~3));
 }
 
 int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan) {
@@ -686,6 +729,7 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.m = matrix;
     p.tile_ad = tile_ad;
     p.n_tiles = (T + kTileRows - 1) / kTileRows;
+    p.work = tile_ad ? sgmv_plan_work(pool, matrix, T, plan) : nullptr;
     const size_t smem = (size_t)(3 * p.n_ids + 3 * S + 1 + kPlanThreads / 32 + 2) * 4;
     static size_t configured = 0;
     if (smem > configured) {
@@ -701,10 +745,12 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
 
 int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool skip_fused) {
     ShrinkParams p;
+    p.skip_fused = skip_fused;
     p.pv = pool->view();
-    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
+    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan,
+                       skip_fused && plan ? sgmv_plan_work(pool, matrix, T, const_cast<int *>(plan)) : nullptr};
     p.m = matrix;
     p.h_in = h_in;
     p.npc = std::min(32, (pool->max_rank + 15) / 16 * 16);
@@ -732,7 +778,8 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
                        cudaStream_t st, const int *tile_ad) {
     ExpandParams p;
     p.pv = pool->view();
-    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
+    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan,
+                       tile_ad && plan ? sgmv_plan_work(pool, matrix, T, const_cast<int *>(plan)) : nullptr};
     p.m = matrix;
     p.h_out = h_out;
     p.kpc = std::min(64, (pool->max_rank + 15) / 16 * 16);

@@ -32,7 +32,7 @@ LORA_DEV_BAD_ADAPTER = 1
 LORA_DEV_BAD_SEGMENTS = 2
 LORA_DEV_WAIT_TIMEOUT = 4
 
-LORA_NOALLOC_SCRATCH_BYTES = 4 << 20
+LORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 EXPORTS = ["lora_pool_create", "lora_pool_destroy", "lora_pool_load", "lora_pool_unload",
            "lora_pool_free_pages", "lora_sgmv_shrink", "lora_sgmv_expand", "lora_bgmv",
