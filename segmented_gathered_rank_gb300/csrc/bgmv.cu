@@ -12,10 +12,9 @@
 //   1. every CTA loads the id list and (for the adapter its cluster index
 //      names) the page-table record, and starts 16-byte asynchronous copies
 //      of its slice of that adapter's A_T and B pages into shared memory;
-//   2. the item's token list is the ordered set of tokens with that id; CTA
-//      rank 0's view of the item is broadcast through distributed shared
-//      memory, so every CTA of the cluster takes the same branches and
-//      reaches the same cluster barriers;
+//   2. the item's token list is the ordered set of tokens with that id;
+//      every CTA of the cluster derives it from the same ids and table, so
+//      all take the same branches (the exchange waits are bounded anyway);
 //   3. x slices of the item's tokens arrive by 16-byte async copies; each
 //      CTA forms partial v over its h_in slice on the tensor cores
 //      (mma.sync m16n8k16, bf16 -> fp32: 16 tokens x 16 ranks x 64 k per
@@ -63,6 +62,17 @@ struct Item {
     float scale;
     int tok[kTok];
 };
+
+// Byte sizes of the shared regions that two buffers share (see the kernel).
+struct BgmvLayout {
+    int a_bytes;    // A_T chunk / warp partials
+    int xy_bytes;   // x and y tiles / id list and histogram
+};
+__host__ __device__ inline BgmvLayout bgmv_layout(int slice_in, int slice_out, int T, int n_ids) {
+    const int a = kJ * (slice_in + 8) * 2, red = kWarps * kTok * kJ * 4;
+    const int xy = kTok * (slice_in + 8) * 2 + kTok * (slice_out + 8) * 2, ids = ((T + n_ids + 1) * 4 + 15) & ~15;
+    return BgmvLayout{a > red ? a : red, xy > ids ? xy : ids};
+}
 
 struct BgmvParams {
     PoolView pv;
@@ -216,23 +226,28 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const PoolView &pv = p.pv;
 
-    // ---- shared memory carve-up (row pitches padded by 16 B for conflict-free ldmatrix)
+    // ---- shared memory carve-up (row pitches padded by 16 B for conflict-free
+    //      ldmatrix).  Regions whose lifetimes do not overlap share space: the
+    //      warps' partial sums live over A_T's chunk once the shrink has read it,
+    //      and the id list / histogram over the x and y tiles, which are loaded
+    //      only after the item's tokens are known.
     const int pin = p.slice_in + 8, pout = p.slice_out + 8;
+    const BgmvLayout L = bgmv_layout(p.slice_in, p.slice_out, p.T, p.n_ids);
     __nv_bfloat16 *sA = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [kJ][pin]   rows of A_T
-    __nv_bfloat16 *sB = sA + kJ * pin;                                   // [kJ][pout]  rows of B
+    float *red = reinterpret_cast<float *>(smem_raw);                    // [kWarps][kTok*kJ] (over sA)
+    __nv_bfloat16 *sB = reinterpret_cast<__nv_bfloat16 *>(smem_raw + L.a_bytes);   // [kJ][pout] rows of B
     __nv_bfloat16 *sX = sB + kJ * pout;                                  // [kTok][pin] rows of x
     __nv_bfloat16 *sY = sX + kTok * pin;                                 // [kTok][pout] rows of y
-    __nv_bfloat16 *sVh = sY + kTok * pout;                               // [kTok][kVPitch] v high part
-    __nv_bfloat16 *sVl = sVh + kTok * kVPitch;                           // [kTok][kVPitch] v residual
-    float *red = reinterpret_cast<float *>(sVl + kTok * kVPitch);        // [kWarps][kTok*kJ]
-    float *recv = red + kWarps * kTok * kJ;                              // [kC][kTok*kJ] partials of every CTA
-    uint64_t *bars = reinterpret_cast<uint64_t *>(recv + kC * kTok * kJ); // [0] partials in, [1] partials consumed
-    int *sids = reinterpret_cast<int *>(bars + 2);                       // [T]
+    int *sids = reinterpret_cast<int *>(sX);                             // [T] (over sX, sY)
     int *hist = sids + p.T;                                              // [n_ids + 1]
-    int *rec = hist + p.n_ids + 1;                                       // [rec_ints]
+    __nv_bfloat16 *sVh = reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(sX) + L.xy_bytes);
+    __nv_bfloat16 *sVl = sVh + kTok * kVPitch;                           // [kTok][kVPitch] v residual
+    float *recv = reinterpret_cast<float *>(sVl + kTok * kVPitch);       // [kC][kTok*kJ] partials of every CTA
+    uint64_t *bars = reinterpret_cast<uint64_t *>(recv + kC * kTok * kJ); // [0] partials in, [1] partials consumed
+    int *rec = reinterpret_cast<int *>(bars + 2);                        // [rec_ints]
     int *warp_tot = rec + pv.rec_ints;                                   // [kWarps + 2]
     Item *mine = reinterpret_cast<Item *>(warp_tot + kWarps + 2);
-    Item *item = mine + 1;
+    const Item *item;
 
     // ---- 1. before the previous kernel on the stream has finished: this
     //         cluster's page-table record and its first rows of pages.  Only
@@ -282,6 +297,15 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
         r_own = min(max(rec[0], 0), pv.max_rank);
         prefetch_pages(r_own, 0);
     }
+    // the exchange barriers, published to the cluster before any CTA touches a peer
+    // (the matching wait comes right before the first remote access)
+    if (tid == 0) {
+        mbar_init(&bars[0], kC);
+        mbar_init(&bars[1], kC);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
 
     // ---- 2. inputs that earlier stream work may produce: wait for it
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -330,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
         }
     }
 
-    // ---- 3. this CTA's view of the item; start its x and y loads at once
+    // ---- 3. the item: every CTA of the cluster derives the same one from the
+    //         same ids and table, so all take the same branches; start its x
+    //         and y loads at once
     int ntok = 0;
     if (a >= 0) ntok = collect_tokens(sids, p.T, a, c, mine->tok, warp_tot);
     if (tid == 0) {
@@ -369,34 +395,13 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
         load_x(mine, ntok);
         load_y(mine, ntok);
     }
-    if (tid == 0) {
-        mbar_init(&bars[0], kC);
-        mbar_init(&bars[1], kC);
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-
-    // ---- 4. rank 0's view is the cluster's: every CTA takes the same branches
-    cluster.sync();
-    {
-        const int *src = reinterpret_cast<const int *>(cluster.map_shared_rank(mine, 0));
-        int *dst = reinterpret_cast<int *>(item);
-        for (int i = tid; i < (int)(sizeof(Item) / sizeof(int)); i += kThreads) dst[i] = src[i];
-    }
-    __syncthreads();
+    item = mine;
     const int ia = item->a, intok = min(max(item->ntok, 0), kTok);
     if (ia < 0 || intok == 0 || item->rank < 0) {
         if (ia >= 0 && intok > 0 && crank == 0 && tid == 0) flag(pv.status, LORA_DEV_BAD_ADAPTER);
-        cluster.sync();        // rank 0's item is read everywhere before any CTA exits
+        asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
         cp_async_wait_all();   // no copy may still be landing when the CTA exits
         return;
-    }
-    bool same = ia == a && intok == ntok;
-    for (int i = 0; i < intok && same; ++i) same = item->tok[i] == mine->tok[i];
-    if (!same) {               // only when the inputs changed under the kernel
-        cp_async_wait_all();
-        __syncthreads();
-        load_x(item, intok);
-        load_y(item, intok);
     }
     const int rank = min(item->rank, pv.max_rank);
     const float scale = item->scale;
@@ -429,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
                 mma16816(d0, a0, a1, a2, a3, b0, b1);
                 mma16816(d1, a0, a1, a2, a3, b2, b3);
             }
+            __syncthreads();     // every warp is done with sA: the partials overwrite it
             float *rw = red + warp * kTok * kJ;
             rw[g * kJ + 2 * q] = d0[0];
             rw[g * kJ + 2 * q + 1] = d0[1];
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) part += red[w * kTok * kJ + tid];   // kThreads == kTok * kJ
             // push this CTA's partial into every CTA's receive slot, then signal them
+            if (jc == 0) asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");   // peers' barriers exist
             if (jc > 0 && !wait_bar(&bars[1], (uint32_t)(jc - 1) & 1u)) failed = true;
             if (!failed) {
 #pragma unroll
@@ -555,10 +562,10 @@ int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, 
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.ids = token_adapter;
-    const size_t smem = (size_t)kJ * (p.slice_in + 8) * 2 + (size_t)kJ * (p.slice_out + 8) * 2 +
-                        (size_t)kTok * (p.slice_in + 8) * 2 + (size_t)kTok * (p.slice_out + 8) * 2 +
-                        (size_t)2 * kTok * kVPitch * 2 + (size_t)(kWarps + kC) * kTok * kJ * 4 + 16 +
-                        (size_t)(T + n_ids + 1 + p.pv.rec_ints + kWarps + 2) * 4 + 2 * sizeof(Item) + 64;
+    const BgmvLayout lay = bgmv_layout(p.slice_in, p.slice_out, T, n_ids);
+    const size_t smem = (size_t)lay.a_bytes + (size_t)kJ * (p.slice_out + 8) * 2 + (size_t)lay.xy_bytes +
+                        (size_t)2 * kTok * kVPitch * 2 + (size_t)kC * kTok * kJ * 4 + 16 +
+                        (size_t)(p.pv.rec_ints + kWarps + 2) * 4 + sizeof(Item) + 16;
     static size_t configured = 0;
     if (smem > configured) {
         if (cudaFuncSetAttribute(bgmv_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=

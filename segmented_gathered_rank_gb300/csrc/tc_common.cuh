@@ -50,20 +50,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Iterations of try_wait before a wait gives up (each try_wait itself blocks
-// for a hardware-defined interval); a healthy pipeline never comes close.
-constexpr uint32_t kSpinLimit = 1u << 24;
-
-// Waits for the phase of `parity` to complete.  Returns false if it gave up
-// (the limit ran out, or another role raised *abort).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort) return false;
-    }
-    return false;
-}
-
 __device__ __forceinline__ unsigned long long now_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
