@@ -133,6 +133,23 @@ __device__ __forceinline__ void remote_arrive(uint64_t *bar, int rank) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(ra) : "memory");
 }
 
+// Store `v` into the float at the same offset as `dst` in CTA `rank` of the
+// cluster; the store completes as a transaction of 4 bytes on that CTA's
+// barrier at the offset of `bar`.
+__device__ __forceinline__ void store_async_remote(float *dst, float v, uint64_t *bar, int rank) {
+    uint32_t rd, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(rd) : "r"(smem_u32(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n" ::"r"(rd),
+                 "r"(__float_as_uint(v)), "r"(rb)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 // Bounded wait (acquire, cluster scope) for the phase of `parity`; false after 2 s.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity) {
     unsigned long long t0, t;
@@ -300,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
     // the exchange barriers, published to the cluster before any CTA touches a peer
     // (the matching wait comes right before the first remote access)
     if (tid == 0) {
-        mbar_init(&bars[0], kC);
+        mbar_init(&bars[0], 1);        // own arrival with the expected bytes; the partials come as transactions
         mbar_init(&bars[1], kC);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -453,16 +470,15 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
             // push this CTA's partial into every CTA's receive slot, then signal them
             if (jc == 0) asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");   // peers' barriers exist
             if (jc > 0 && !wait_bar(&bars[1], (uint32_t)(jc - 1) & 1u)) failed = true;
+            // asynchronous remote stores that count their bytes on the receiver's barrier
             if (!failed) {
 #pragma unroll
-                for (int r = 0; r < kC; ++r) *cluster.map_shared_rank(recv + crank * kTok * kJ + tid, r) = part;
+                for (int r = 0; r < kC; ++r) store_async_remote(recv + crank * kTok * kJ + tid, part, &bars[0], r);
             }
-            asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
+            // this CTA's own phase: it expects every CTA's partial (kC x kTok x kJ floats)
+            if (tid == 0) mbar_arrive_expect_tx(&bars[0], (uint32_t)(kC * kTok * kJ * sizeof(float)));
         }
-        __syncthreads();
         if (jc == 0) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-        if (tid == 0 && !failed)
-            for (int r = 0; r < kC; ++r) remote_arrive(&bars[0], r);
         if (!failed && !wait_bar(&bars[0], (uint32_t)jc & 1u)) failed = true;
         if (__syncthreads_or(failed)) {
             if (tid == 0) flag(pv.status, LORA_DEV_WAIT_TIMEOUT);
