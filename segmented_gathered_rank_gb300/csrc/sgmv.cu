@@ -31,8 +31,8 @@ static_assert(kM == 32, "an item's tokens are collected one per lane of a warp")
 constexpr int kKs = 128;          // k per shrink pipeline stage
 constexpr int kStagesS = 4;
 constexpr int kNb = 128;          // output columns per expand block
-constexpr int kBlocksPerUnit = 4; // column blocks per expand unit (512 columns)
-constexpr int kStagesE = 3;
+constexpr int kMaxBlocksPerUnit = 8; // column blocks per expand unit (up to 1024 columns)
+constexpr int kStagesE = 4;
 constexpr int kMaxS = 8192;       // segments the segment-mode kernels take
 constexpr int kPlanThreads = 1024;
 constexpr int kTileRows = kFuseTileRows;   // M-tile rows of the tensor-core GEMM
@@ -486,9 +486,9 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
 }
 
 // ---------------------------------------------------------------------------
-// Expand: 128 threads, unit = (item, up to kBlocksPerUnit column blocks of
+// Expand: 128 threads, unit = (item, up to bpu <= kMaxBlocksPerUnit column blocks of
 // kNb).  warp w: rows 16*(w & 1) .. +16, columns 64*(w >> 1) .. +64 of the
-// block.  y tiles and B chunks stream through a 3-stage pipeline; y is read
+// block.  y tiles and B chunks stream through a kStagesE-stage pipeline; y is read
 // and written with coalesced 16-byte accesses staged in shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kThreadsE = 128;
@@ -502,6 +502,7 @@ struct ExpandParams {
     int ld_v;
     __nv_bfloat16 *y;
     int ncg;       // column groups per item
+    int bpu;       // column blocks per unit (1 .. kMaxBlocksPerUnit)
     const int *tile_ad;   // non-null: the plan's item masks name rows whose term the GEMM already added
 };
 
@@ -555,8 +556,8 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     const int r = min(r_rec, p.ld_v);
     const float scale = __int_as_float(rec[1]);
     const int nb_total = (p.h_out + kNb - 1) / kNb;
-    const int b_first = cg * kBlocksPerUnit;
-    const int nb = min(kBlocksPerUnit, nb_total - b_first);
+    const int b_first = cg * p.bpu;
+    const int nb = min(p.bpu, nb_total - b_first);
     if (nb <= 0 || r <= 0) return;
     const int mg = warp & 1, nh = warp >> 1;
     const int g = lane >> 2, q = lane & 3;
@@ -788,7 +789,11 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.tile_ad = tile_ad;
     const int nb_total = (h_out + kNb - 1) / kNb;
-    p.ncg = (nb_total + kBlocksPerUnit - 1) / kBlocksPerUnit;
+    // wide units amortise each unit's start-up latency (measured: fewer, longer
+    // CTAs win even when the grid is below the resident-CTA count); a plan's
+    // compacted work list (many tiny decode items) keeps narrower units
+    p.bpu = tile_ad ? 4 : kMaxBlocksPerUnit;
+    p.ncg = (nb_total + p.bpu - 1) / p.bpu;
     const size_t smem = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
                         (size_t)(kM + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
     static size_t configured = 0;
