@@ -193,9 +193,8 @@ int lora_layer_forward(lora_pool *pool, int matrix, const void *x, const void *W
  * LORA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library keeps until the process exits.  Requires
  * lora_layer_forward_workspace_size(pool, matrix, S, T) <=
- * LORA_NOALLOC_SCRATCH_BYTES (about 5 * T * max_rank * 4 bytes -- v and the
- * tensor-core shrink's four K-split partials -- plus a small per-token plan;
- * else LORA_ERR_ARG) and the pool's device to be current
+ * LORA_NOALLOC_SCRATCH_BYTES (about T * max_rank * 4 bytes plus a small
+ * per-token plan; else LORA_ERR_ARG) and the pool's device to be current
  * (else LORA_ERR_ARG).  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress); make
  * that first call before any stream capture.  All calls share the array:

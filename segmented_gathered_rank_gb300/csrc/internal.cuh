@@ -72,6 +72,7 @@ struct lora_pool {
     std::vector<int> mat_h_in;        // per matrix, -1 until the first load
     std::vector<int> mat_h_out;
     std::vector<int> mat_n_ids;       // per matrix: 1 + largest adapter id ever loaded
+    std::vector<int> mat_max_rank;    // per matrix: largest rank ever loaded
     // load staging: pinned host buffer -> device buffer -> scatter kernel
     void *h_stage;
     void *d_stage;
@@ -206,10 +207,12 @@ bool sgmv_shrink_ok(const lora_pool *pool, int h_in, int S);
 bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S);
 // plan: nullptr (items from the segment table) or a plan from launch_sgmv_plan
 // skip_fused: the plan's item masks name rows whose v the tensor-core shrink computes; items
-// all of whose rows are such rows are skipped.
+// all of whose rows are such rows are skipped.  tc_min_rows > 0 (segment tables): items of
+// segments the tensor-core shrink takes (that many rows or more, rank kShrinkTcSegMinRank..kFuseMaxRank)
+// are skipped.
 int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
-                       cudaStream_t st, bool skip_fused = false);
+                       cudaStream_t st, bool skip_fused = false, int tc_min_rows = 0);
 int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float *v, int ld_v, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
                        cudaStream_t st, const int *tile_ad = nullptr);
@@ -224,17 +227,25 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
 int num_sms();   // SMs of the current device (cached)
 bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
 // tile_ad != nullptr: M-tiles with tile_ad[m] >= 0 also get that adapter's term
-// s * v . B inside the GEMM, v being the sum of the nsplit partials
-// v[s][T][ld_v] that launch_shrink_tc wrote.
+// s * v . B (v: T x ld_v fp32) inside the GEMM.
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
                    cudaStream_t st, int matrix = 0, const int *tile_ad = nullptr, const float *v = nullptr,
-                   int ld_v = 0, int nsplit = 1);
-// K splits of the tensor-core shrink (at most kShrinkTcSplits).
+                   int ld_v = 0);
+// Tensor-core shrink (tcgen05) of 128-row tiles that share one adapter of
+// rank 1..kFuseMaxRank: the fused layer's uniform M-tiles (tile_ad), or, for
+// a segment table, 128-row pieces of the segments with at least
+// kShrinkTcMinRows rows and rank at least kShrinkTcSegMinRank (measured: at
+// lower ranks the warp-MMA shrink is as fast, both being bound by reading x,
+// and a second launch only adds latency; the warp-MMA SGMV shrink skips the
+// segments taken here).  K is split over up to
+// kShrinkTcSplits CTAs of a cluster.
 constexpr int kShrinkTcSplits = 4;
-int shrink_tc_splits(int h_in);
-// v partials [shrink_tc_splits(h_in)][T][ld_v] of the M-tiles with tile_ad[m] >= 0.
+constexpr int kShrinkTcMinRows = 64;
+constexpr int kShrinkTcSegMinRank = 65;
+constexpr int kShrinkTcMaxS = 8192;
+bool shrink_tc_ok(const lora_pool *pool, int h_in, int S);
 int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, const int *tile_ad,
-                     float *vpart, int ld_v, cudaStream_t st);
+                     const int *seg_starts, const int *seg_adapter, int S, float *v, int ld_v, cudaStream_t st);
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st);
 int launch_base_gemm(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y,

@@ -51,10 +51,8 @@ struct LayerTcParams {
     const int *tile_ad;     // per M-tile: adapter whose term is added here, or -1
     PoolView pv;
     int m;
-    const float *v;         // [nsplit][T][ld_v]: K-split partial sums of x . A_a for the fused tiles' rows
+    const float *v;         // [T][ld_v]: x . A_a of the fused tiles' rows
     int ld_v;
-    int nsplit;
-    long long split_stride; // floats between partials
 };
 
 template <int ST>
@@ -121,29 +119,24 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
         const bool live = row < p.T;
         const float *vrow = p.v + (long long)(live ? row : 0) * p.ld_v + j0;
         const bool vec = (p.ld_v & 3) == 0;
-        // 8 ranks at a time: the K-split partials added in a fixed order (deterministic)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             if (c * 8 >= kpad) break;
             float vv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) vv[e] = 0.f;
             const float *vp = vrow + c * 8;
-            for (int sp = 0; sp < p.nsplit; ++sp, vp += p.split_stride) {
-                if (vec) {
+            if (vec) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float4 f = (live && c * 8 + 4 * h < rn) ? *reinterpret_cast<const float4 *>(vp + 4 * h)
-                                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                        vv[4 * h] += f.x;
-                        vv[4 * h + 1] += f.y;
-                        vv[4 * h + 2] += f.z;
-                        vv[4 * h + 3] += f.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) vv[e] += (live && c * 8 + e < rn) ? vp[e] : 0.f;
+                for (int h = 0; h < 2; ++h) {
+                    const float4 f = (live && c * 8 + 4 * h < rn) ? *reinterpret_cast<const float4 *>(vp + 4 * h)
+                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    vv[4 * h] = f.x;
+                    vv[4 * h + 1] = f.y;
+                    vv[4 * h + 2] = f.z;
+                    vv[4 * h + 3] = f.w;
                 }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vv[e] = (live && c * 8 + e < rn) ? vp[e] : 0.f;
             }
             uint4 hi4, lo4;
             __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(&hi4);
@@ -398,41 +391,52 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Shrink of the fused M-tiles on the tensor cores.  For an M-tile whose 128
-// rows all use adapter a (rank r <= kFuseMaxRank) the shrink is a dense
-// contraction v = x[tile] . A_a^T with M = 128, N = r, K = h_in; at rank 128
-// that is 256 flops per x element, more than warp-level MMAs sustain at HBM
-// rate.  Grid (M-tiles, K splits); a CTA whose tile is not fused exits at
-// once.  Through a 6-stage ring, warp 0 streams x (one 128 x 64 TMA box,
-// 128-byte swizzle) and warps 2-5 the r page rows of A_a (16-byte cp.async
-// into the same swizzled K-major layout, each thread's copies arriving on the
-// stage's mbarrier as they land); warp 1 issues tcgen05.mma (M 128, N = r
-// rounded up to 16) into TMEM; then warps 2-5 read the accumulator and store
-// the split's partial sums, which the GEMM adds in a fixed order.
+// Shrink on the tensor cores for tiles of up to 128 rows that share one
+// adapter: v[rows] = x[rows] . A_a^T, M = 128, N = r (<= kFuseMaxRank),
+// K = h_in.  At rank 128 that is 256 flops per x element, more than
+// warp-level MMAs sustain at HBM rate.  A tile is either an M-tile of the
+// fused layer whose rows all use one adapter (the plan's tile array), or
+// 128 consecutive rows of one long segment of a segment table (long
+// prefill segments, encoder sequences).
+//
+// Grid (tiles, K splits); the nsplit CTAs of a tile form a cluster.
+// Through a ring of shared-memory stages, warp 0 streams x (one 128 x 64 TMA
+// box, 128-byte swizzle) and warps 2-5 the r page rows of A_a (16-byte
+// cp.async into the same swizzled K-major layout, each thread's copies
+// arriving on the stage's mbarrier as they land); warp 1 issues tcgen05.mma
+// into TMEM.  The splits' partial accumulators then meet in the first CTA of
+// the cluster: the others read theirs out of TMEM and send them with
+// asynchronous remote stores counted on its mbarrier; it adds them, in split
+// order, to its own and stores v.  Rows of a tile past its end (another
+// segment's, or past T) are computed and dropped.
 // ---------------------------------------------------------------------------
-constexpr int SK_STAGES = 6;
+constexpr int SK_MAX_STAGES = 8;
 constexpr int SK_X_BYTES = BM * BK * 2;
-constexpr int SK_A_BYTES = kFuseMaxRank * BK * 2;
-constexpr int SK_STAGE_BYTES = SK_X_BYTES + SK_A_BYTES;
 constexpr uint32_t SK_TMEM_COLS = kFuseMaxRank;
 
 struct ShrinkTcParams {
     int T, num_k, nsplit;
-    const int *tile_ad;
+    int stages, stage_bytes;   // ring depth; bytes of one stage (x tile + npad_max A rows)
+    const int *tile_ad;        // fused layer: per M-tile adapter (or -1); else nullptr
+    const int *seg_starts, *seg_adapter;   // segment tables: tiles of segments with >= min_rows rows
+    int S, min_rows;
     PoolView pv;
     int m;
-    float *vpart;           // [nsplit][T][ld_v]
+    float *v;
     int ld_v;
-    long long split_stride;
     int *status;
 };
 
 struct SkCtrl {
-    uint64_t full[SK_STAGES];
-    uint64_t empty[SK_STAGES];
-    uint64_t done;
+    uint64_t full[SK_MAX_STAGES];
+    uint64_t empty[SK_MAX_STAGES];
+    uint64_t done;    // every MMA of the CTA complete
+    uint64_t ready;   // (other splits) the first CTA may receive
+    uint64_t recv;    // (first CTA) every other split's partial has arrived
     uint32_t tmem_base;
     int abort;
+    int tile[3];      // adapter, first row, rows
+    int wsum[kThreadsTC / 32 + 1];
     int page[kFuseMaxRank];
 };
 
@@ -446,29 +450,145 @@ __device__ __forceinline__ void cp_async_arrive_sk(uint64_t *bar) {
 }
 __device__ __forceinline__ void cp_wait_all_sk() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+__device__ __forceinline__ uint32_t cluster_rank_sk() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t mapa_sk(const void *p, int rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ void remote_arrive_sk(uint64_t *bar, int rank) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(mapa_sk(bar, rank)) : "memory");
+}
+// 16 bytes into the first CTA's shared memory, counted on its barrier `bar`.
+__device__ __forceinline__ void st_async16_sk(uint32_t dst, uint32_t bar, float a, float b, float c, float d) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(dst),
+                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+                 "r"(bar)
+                 : "memory");
+}
+// Bounded cluster-scope acquire wait (the remote arrivals and transactions release at cluster scope).
+__device__ __forceinline__ bool wait_cluster_sk(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    const unsigned long long t0 = now_ns();
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n"
+            "}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 63u) == 63u) {
+            if (abort && *abort) return false;
+            if (now_ns() - t0 > kTimeoutNs) return false;
+        }
+    }
+}
+
+// Segment tables: tile `t` among the 128-row pieces of the segments with at
+// least min_rows rows.  All threads call it; ctrl->tile gets the result.
+__device__ void segment_tile_sk(const ShrinkTcParams &p, int t, int *scan, SkCtrl *ctrl) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = kThreadsTC / 32;
+    const int per = (p.S + kThreadsTC - 1) / kThreadsTC;
+    const int lo = min(p.S, tid * per), hi = min(p.S, lo + per);
+    int sum = 0;
+    for (int s = lo; s < hi; ++s) {
+        const int b = min(max(p.seg_starts[s], 0), p.T), e = min(max(p.seg_starts[s + 1], 0), p.T);
+        const int n = e - b >= p.min_rows ? (e - b + BM - 1) / BM : 0;
+        scan[s] = n;
+        sum += n;
+    }
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) ctrl->wsum[warp] = inc;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int v = ctrl->wsum[w];
+            ctrl->wsum[w] = run;
+            run += v;
+        }
+        ctrl->wsum[NW] = run;
+    }
+    __syncthreads();
+    int run = ctrl->wsum[warp] + inc - sum;
+    for (int s = lo; s < hi; ++s) {
+        const int v = scan[s];
+        scan[s] = run;
+        run += v;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int a = -1, row0 = 0, rows = 0;
+        if (t < ctrl->wsum[NW]) {
+            int l = 0, h = p.S - 1;            // last segment whose first tile index <= t
+            while (l < h) {
+                const int mid = (l + h + 1) >> 1;
+                if (scan[mid] <= t) l = mid; else h = mid - 1;
+            }
+            const int b = min(max(p.seg_starts[l], 0), p.T), e = min(max(p.seg_starts[l + 1], 0), p.T);
+            a = p.seg_adapter[l];
+            row0 = b + (t - scan[l]) * BM;
+            rows = min(BM, e - row0);
+        }
+        ctrl->tile[0] = a;
+        ctrl->tile[1] = row0;
+        ctrl->tile[2] = rows;
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreadsTC, 1)
     shrink_tc_kernel(const __grid_constant__ CUtensorMap tmx, ShrinkTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SkCtrl *ctrl = reinterpret_cast<SkCtrl *>(smem + SK_STAGES * SK_STAGE_BYTES);
+    SkCtrl *ctrl = reinterpret_cast<SkCtrl *>(smem + p.stages * p.stage_bytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mb = blockIdx.x, split = blockIdx.y;
-    const int a = p.tile_ad[mb];
-    if (a < 0 || a >= p.pv.max_adapters) return;
+    const int split = p.nsplit > 1 ? (int)cluster_rank_sk() : 0;
+    int a, row0, rows;
+    if (p.tile_ad) {
+        row0 = blockIdx.x * BM;
+        rows = min(BM, p.T - row0);
+        a = rows > 0 ? p.tile_ad[blockIdx.x] : -1;
+    } else {
+        segment_tile_sk(p, blockIdx.x, reinterpret_cast<int *>(smem), ctrl);
+        a = ctrl->tile[0];
+        row0 = ctrl->tile[1];
+        rows = ctrl->tile[2];
+    }
+    // every CTA of the cluster resolves the same tile, so they leave together
+    if (a < 0 || a >= p.pv.max_adapters || rows <= 0) return;
     const int *rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
     const int r = rec[0];
-    if (r < 1 || r > kFuseMaxRank || r > p.ld_v) return;     // the GEMM adds nothing for such a tile either
+    if (r < (p.tile_ad ? 1 : kShrinkTcSegMinRank) || r > kFuseMaxRank || r > p.ld_v) return;   // the warp-MMA shrink takes it
     const int npad = (r + 15) & ~15;
     const uint32_t idesc = idesc_bf16_f32(BM, npad);
     const int kb0 = split * p.num_k / p.nsplit, kb1 = (split + 1) * p.num_k / p.nsplit;
     volatile int *abort = &ctrl->abort;
+    const int ST = p.stages;
 
+    __syncthreads();                       // the segment scan (aliasing the ring) is done
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SK_STAGES; ++s) {
+        for (int s = 0; s < ST; ++s) {
             mbar_init(&ctrl->full[s], 129);    // the x TMA (with its bytes) + 128 threads' A copies
             mbar_init(&ctrl->empty[s], 1);
         }
         mbar_init(&ctrl->done, 1);
+        mbar_init(&ctrl->ready, 1);
+        mbar_init(&ctrl->recv, 1);
         ctrl->abort = 0;
         mbar_fence_init();
         prefetch_tmap(&tmx);
@@ -484,6 +604,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    if (p.nsplit > 1) asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
     const uint32_t tmem = ctrl->tmem_base;
 
     if (warp == 0) {
@@ -492,14 +613,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             int issued = 0;
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
-                const int i = kb - kb0, stage = i % SK_STAGES;
-                const uint32_t phase = (uint32_t)(i / SK_STAGES) & 1u;
+                const int i = kb - kb0, stage = i % ST;
+                const uint32_t phase = (uint32_t)(i / ST) & 1u;
                 if (!wait_phase(&ctrl->empty[stage], phase ^ 1u, abort)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&ctrl->full[stage], (uint32_t)SK_X_BYTES);
-                tma_load_2d(smem + stage * SK_STAGE_BYTES, &tmx, kb * BK, mb * BM, &ctrl->full[stage]);
+                tma_load_2d(smem + stage * p.stage_bytes, &tmx, kb * BK, row0, &ctrl->full[stage]);
                 ++issued;
             }
             if (!ok) {
@@ -507,8 +628,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 __threadfence_block();
                 flag(p.status, LORA_DEV_WAIT_TIMEOUT);
                 // the x copies still landing must land before exit (the A copies arrive by themselves)
-                for (int i = issued > SK_STAGES ? issued - SK_STAGES : 0; i < issued; ++i)
-                    wait_phase(&ctrl->full[i % SK_STAGES], (uint32_t)(i / SK_STAGES) & 1u, nullptr);
+                for (int i = issued > ST ? issued - ST : 0; i < issued; ++i)
+                    wait_phase(&ctrl->full[i % ST], (uint32_t)(i / ST) & 1u, nullptr);
             }
         }
         __syncwarp();
@@ -517,15 +638,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (lane == 0) {
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
-                const int i = kb - kb0, stage = i % SK_STAGES;
-                const uint32_t phase = (uint32_t)(i / SK_STAGES) & 1u;
+                const int i = kb - kb0, stage = i % ST;
+                const uint32_t phase = (uint32_t)(i / ST) & 1u;
                 if (!wait_phase(&ctrl->full[stage], phase, abort)) {
                     ok = false;
                     break;
                 }
                 fence_proxy_async();                  // the A rows came through the generic proxy
                 fence_after_sync();
-                const uint32_t a0 = smem_u32(smem + stage * SK_STAGE_BYTES);
+                const uint32_t a0 = smem_u32(smem + stage * p.stage_bytes);
                 const uint32_t b0 = a0 + SK_X_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
@@ -548,10 +669,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // thread's copies of a stage arrive on the stage's barrier when they land.
         const int t = threadIdx.x - 64, c = t & 7;
         for (int kb = kb0; kb < kb1; ++kb) {
-            const int i = kb - kb0, stage = i % SK_STAGES;
-            const uint32_t phase = (uint32_t)(i / SK_STAGES) & 1u;
+            const int i = kb - kb0, stage = i % ST;
+            const uint32_t phase = (uint32_t)(i / ST) & 1u;
             if (!wait_phase(&ctrl->empty[stage], phase ^ 1u, abort)) break;
-            const uint32_t sa = smem_u32(smem + stage * SK_STAGE_BYTES + SK_X_BYTES);
+            const uint32_t sa = smem_u32(smem + stage * p.stage_bytes + SK_X_BYTES);
             for (int j = t >> 3; j < r; j += 16)
                 cp_async16_sk(sa + swz128(j, c), page_row<__nv_bfloat16>(p.pv, ctrl->page[j]) + kb * BK + c * 8);
             cp_async_arrive_sk(&ctrl->full[stage]);
@@ -559,26 +680,74 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         cp_wait_all_sk();                            // nothing lands after the CTA exits
 
         const int sub = warp & 3;
-        const bool ok = wait_phase(&ctrl->done, 0, nullptr) && !*abort;
-        if (__all_sync(0xffffffffu, ok)) {
-            fence_after_sync();
-            const int row = mb * BM + sub * 32 + lane;
-            float *out = p.vpart + (long long)split * p.split_stride + (long long)row * p.ld_v;
-            const bool vec = (p.ld_v & 3) == 0;
-            for (int c0 = 0; c0 < npad; c0 += 32) {
-                float f[32];
-                __syncwarp();
-                tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
-                if (row < p.T) {
-                    if (vec) {
+        const int lrow = sub * 32 + lane;            // row of the tile (TMEM lane)
+        bool ok = wait_phase(&ctrl->done, 0, nullptr) && !*abort;
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) fence_after_sync();
+        const int pitch = npad + 4;                  // floats per received row (16-byte aligned, v4 conflict-free)
+        float *recvbuf = reinterpret_cast<float *>(smem);   // [nsplit - 1][BM][pitch], over the drained ring
+        if (p.nsplit > 1) asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+        if (p.nsplit > 1 && split > 0) {
+            // send this split's partial to the first CTA once it can receive
+            ok = ok && wait_cluster_sk(&ctrl->ready, 0, abort);
+            if (__all_sync(0xffffffffu, ok)) {
+                const uint32_t rbar = mapa_sk(&ctrl->recv, 0);
+                const uint32_t rdst = mapa_sk(recvbuf + ((long long)(split - 1) * BM + lrow) * pitch, 0);
+                for (int c0 = 0; c0 < npad; c0 += 32) {
+                    float f[32];
+                    __syncwarp();
+                    tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            if (c0 + e < r)   // r <= ld_v and ld_v % 4 == 0: the float4 stays in the row
-                                *reinterpret_cast<float4 *>(out + c0 + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
-                    } else {
+                    for (int e = 0; e < 32; e += 4)
+                        if (c0 + e < npad) st_async16_sk(rdst + (c0 + e) * 4, rbar, f[e], f[e + 1], f[e + 2], f[e + 3]);
+                }
+            } else if (lane == 0) {
+                flag(p.status, LORA_DEV_WAIT_TIMEOUT);
+            }
+        } else {
+            if (p.nsplit > 1) {
+                // the ring is drained (all MMAs complete, all copies landed): open it to the other splits
+                if (threadIdx.x == 64) {
+                    mbar_arrive_expect_tx(&ctrl->recv, (uint32_t)((p.nsplit - 1) * BM * npad * 4));
+                    for (int s = 1; s < p.nsplit; ++s) remote_arrive_sk(&ctrl->ready, s);
+                }
+                ok = ok && wait_cluster_sk(&ctrl->recv, 0, abort);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok && lane == 0) flag(p.status, LORA_DEV_WAIT_TIMEOUT);
+            }
+            if (ok) {
+                const int row = row0 + lrow;
+                float *out = p.v + (long long)row * p.ld_v;
+                const bool vec = (p.ld_v & 3) == 0;
+                for (int c0 = 0; c0 < npad; c0 += 32) {
+                    float f[32];
+                    __syncwarp();
+                    tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
+                    for (int s = 1; s < p.nsplit; ++s) {       // split order: deterministic
+                        const float *src = recvbuf + ((long long)(s - 1) * BM + lrow) * pitch + c0;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (c0 + e < r) out[c0 + e] = f[e];
+                        for (int e = 0; e < 32; e += 4) {
+                            if (c0 + e < npad) {
+                                const float4 q = *reinterpret_cast<const float4 *>(src + e);
+                                f[e] += q.x;
+                                f[e + 1] += q.y;
+                                f[e + 2] += q.z;
+                                f[e + 3] += q.w;
+                            }
+                        }
+                    }
+                    if (lrow < rows) {
+                        if (vec) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                if (c0 + e < r)   // r <= ld_v and ld_v % 4 == 0: the float4 stays in the row
+                                    *reinterpret_cast<float4 *>(out + c0 + e) =
+                                        make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (c0 + e < r) out[c0 + e] = f[e];
+                        }
                     }
                 }
             }
@@ -643,7 +812,7 @@ bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T) {
 }
 
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
-                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v, int nsplit) {
+                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v) {
     CUtensorMap tmx, tmw;
     if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM) || !make_tmap(&tmw, W, (uint64_t)h_in, (uint64_t)h_out, BN))
         return LORA_ERR_CUDA;
@@ -662,41 +831,78 @@ int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, co
     p.m = matrix;
     p.v = v;
     p.ld_v = ld_v;
-    p.nsplit = nsplit;
-    p.split_stride = (long long)T * ld_v;
     if (tile_ad) return launch_gemm_variant<3, true>(tmx, tmw, p, st);
     return launch_gemm_variant<4, false>(tmx, tmw, p, st);
 }
 
-int shrink_tc_splits(int h_in) { return std::max(1, std::min(kShrinkTcSplits, h_in / BK)); }
+bool shrink_tc_ok(const lora_pool *pool, int h_in, int S) {
+    return pool->dtype == LORA_BF16 && h_in % BK == 0 && S <= kShrinkTcMaxS && encode_fn() != nullptr &&
+           num_sms() > 0;
+}
 
 int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, const int *tile_ad,
-                     float *vpart, int ld_v, cudaStream_t st) {
+                     const int *seg_starts, const int *seg_adapter, int S, float *v, int ld_v, cudaStream_t st) {
     CUtensorMap tmx;
     if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM)) return LORA_ERR_CUDA;
     ShrinkTcParams p;
     p.T = T;
     p.num_k = h_in / BK;
-    p.nsplit = shrink_tc_splits(h_in);
+    // K splits: enough CTAs for two per SM over the expected tiles, at least 4
+    // k-blocks per split
+    const int est_tiles = std::max(1, tile_ad ? (T + BM - 1) / BM : T / BM);
+    p.nsplit = std::max(1, std::min({kShrinkTcSplits, p.num_k / 4, 2 * num_sms() / est_tiles}));
     p.tile_ad = tile_ad;
+    p.seg_starts = seg_starts;
+    p.seg_adapter = seg_adapter;
+    p.S = S;
+    p.min_rows = kShrinkTcMinRows;
     p.pv = pool->view();
     p.m = matrix;
-    p.vpart = vpart;
+    p.v = v;
     p.ld_v = ld_v;
-    p.split_stride = (long long)T * ld_v;
     p.status = pool->d_status;
-    const size_t smem = (size_t)SK_STAGES * SK_STAGE_BYTES + sizeof(SkCtrl) + 1024;
-    static bool configured = false;
-    if (!configured) {
+    // ring: stages of an x tile plus the pool's widest A chunk; two CTAs per SM
+    // when the stages and the partials the first CTA of a cluster receives fit
+    // in half the shared memory
+    const int npad_max = std::min(kFuseMaxRank, (pool->max_rank + 15) / 16 * 16);
+    p.stage_bytes = SK_X_BYTES + npad_max * BK * 2;
+    const size_t fixed = sizeof(SkCtrl) + 1024;
+    const size_t need_recv = (size_t)(p.nsplit - 1) * BM * (npad_max + 4) * 4;
+    const size_t need_scan = tile_ad ? 0 : (size_t)(S + 1) * 4;
+    p.stages = 0;
+    for (size_t budget : {(size_t)113 * 1024, (size_t)227 * 1024}) {
+        const int st_n = (int)std::min<size_t>(SK_MAX_STAGES, (budget - fixed) / p.stage_bytes);
+        if (st_n >= 4 && (size_t)st_n * p.stage_bytes >= std::max(need_recv, need_scan)) {
+            p.stages = st_n;
+            break;
+        }
+    }
+    if (p.stages == 0) return LORA_ERR_ARG;       // not reached for ranks <= kFuseMaxRank
+    const size_t smem = (size_t)p.stages * p.stage_bytes + fixed;
+    static size_t configured = 0;
+    if (smem > configured) {
         if (cudaFuncSetAttribute(shrink_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return LORA_ERR_CUDA;
-        configured = true;
+        configured = smem;
     }
-    const dim3 grid((T + BM - 1) / BM, p.nsplit);
-    shrink_tc_kernel<<<grid, kThreadsTC, smem, st>>>(tmx, p);
+    const int tiles = tile_ad ? (T + BM - 1) / BM : T / kShrinkTcMinRows;
+    if (tiles == 0) return LORA_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles, p.nsplit);
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = p.nsplit;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, shrink_tc_kernel, tmx, p);
     count_launch();
-    return cuda_status(cudaGetLastError());
+    return cuda_status(e);
 }
 
 }  // namespace lora

@@ -173,8 +173,17 @@ int launch_bgmv(const lora_pool *p, int matrix, int h_in, int h_out, const void 
 
 int launch_shrink(const lora_pool *p, int matrix, int h_in, const void *x, float *v, int ld_v,
                   const int *seg_starts, const int *seg_adapter, int S, int T, cudaStream_t st) {
-    if (sgmv_shrink_ok(p, h_in, S))
-        return launch_sgmv_shrink(p, matrix, h_in, x, v, ld_v, seg_starts, seg_adapter, S, T, nullptr, st);
+    if (sgmv_shrink_ok(p, h_in, S)) {
+        // long segments on the tensor cores, the rest with warp MMAs
+        int min_rows = 0;
+        if (shrink_tc_ok(p, h_in, S) && p->mat_max_rank[matrix] >= kShrinkTcSegMinRank) {
+            const int rc = launch_shrink_tc(p, matrix, h_in, x, T, nullptr, seg_starts, seg_adapter, S, v, ld_v, st);
+            if (rc) return rc;
+            min_rows = kShrinkTcMinRows;
+        }
+        return launch_sgmv_shrink(p, matrix, h_in, x, v, ld_v, seg_starts, seg_adapter, S, T, nullptr, st, false,
+                                  min_rows);
+    }
     const size_t smem = (size_t)p->max_rank * sizeof(float);
     if (p->dtype == LORA_BF16)
         shrink_token_kernel<__nv_bfloat16><<<T, kThreads, smem, st>>>(

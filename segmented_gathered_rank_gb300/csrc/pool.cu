@@ -76,22 +76,21 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
     const bool tc = gemm_tc_ok(p, h_in, h_out, T);
     if (sgmv_plan_ok(p, matrix, S) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
         // 1. plan: tokens grouped by adapter; GEMM M-tiles whose rows share one adapter
-        // 2. (tensor cores) v of those tiles: K-split partials of M 128 x N r contractions
+        // 2. (tensor cores) v of those tiles: M 128 x N r contractions, K split over a cluster
         // 3. v of every other adapted token (warp-MMA SGMV shrink)
         // 4. base product; the uniform tiles add their low-rank term inside the GEMM
         // 5. expand the remaining rows
-        const size_t vfloats = (size_t)T * p->max_rank;
-        float *vpart = v + vfloats;
-        int *plan = reinterpret_cast<int *>(
-            (reinterpret_cast<uintptr_t>(vpart + (size_t)kShrinkTcSplits * vfloats) + 255) & ~uintptr_t(255));
-        int *tile_ad = tc ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
+        int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
+                                            ~uintptr_t(255));
+        const bool tcs = tc && shrink_tc_ok(p, h_in, S);
+        int *tile_ad = tcs ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
         if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, tile_ad))) return rc;
-        if (tc && (rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, vpart, p->max_rank, st))) return rc;
-        if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st,
-                                     tc)))
+        if (tcs && (rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, nullptr, nullptr, 0, v, p->max_rank, st)))
             return rc;
-        rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, vpart, p->max_rank,
-                                 shrink_tc_splits(h_in))
+        if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st,
+                                     tcs)))
+            return rc;
+        rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank)
                 : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
         if (rc) return rc;
         return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st,
@@ -171,6 +170,7 @@ int lora_pool_create(lora_pool **out, int dtype, int page_elems, int n_pages, in
         p->mat_h_in.assign(n_matrices, -1);
         p->mat_h_out.assign(n_matrices, -1);
         p->mat_n_ids.assign(n_matrices, 0);
+        p->mat_max_rank.assign(n_matrices, 0);
     } catch (...) {
         lora_pool_destroy(p);
         return LORA_ERR_ARG;
@@ -269,6 +269,7 @@ int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale,
     p->mat_h_in[matrix] = h_in;
     p->mat_h_out[matrix] = h_out;
     if (adapter + 1 > p->mat_n_ids[matrix]) p->mat_n_ids[matrix] = adapter + 1;
+    if (rank > p->mat_max_rank[matrix]) p->mat_max_rank[matrix] = rank;
     return LORA_OK;
 }
 
@@ -345,8 +346,7 @@ int lora_bgmv(lora_pool *p, int matrix, const void *x, void *y, const int *token
 size_t lora_layer_forward_workspace_size(const lora_pool *p, int matrix, int S, int T) {
     int h_in, h_out;
     if (!p || T < 0 || S < 0 || matrix_dims(p, matrix, &h_in, &h_out)) return 0;
-    // v, the tensor-core shrink's K-split partials, then (256-byte aligned) the plan
-    return (size_t)T * p->max_rank * sizeof(float) * (1 + kShrinkTcSplits) + sgmv_plan_bytes(p, matrix, T) + 256;
+    return (size_t)T * p->max_rank * sizeof(float) + sgmv_plan_bytes(p, matrix, T) + 256;
 }
 
 int lora_layer_forward(lora_pool *p, int matrix, const void *x, const void *W, void *y,

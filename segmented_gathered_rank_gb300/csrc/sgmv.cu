@@ -141,6 +141,7 @@ __device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int 
             it.a = seg_adapter[lo];
             it.off = beg + c * kM;
             it.nt = min(kM, end - it.off);
+            it.pad = end - beg;           // segment tables: the segment's length
         }
         reinterpret_cast<Item *>(wtot)[0] = it;
     }
@@ -338,6 +339,7 @@ struct ShrinkParams {
     ItemSource src;
     int m, h_in;
     bool skip_fused;   // skip plan items whose rows all sit in tensor-core-shrunk tiles
+    int tc_min_rows;   // > 0: skip segments of at least this many rows the tensor-core shrink takes
     int npc;       // ranks per CTA: max_rank rounded up to 16, at most 32 (grid.y covers the rest)
     const __nv_bfloat16 *x;
     float *v;
@@ -367,6 +369,9 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
         if (((unsigned)it.pad & all) == all) return;
     }
     if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0 && blockIdx.z == 0)) return;
+    if (p.tc_min_rows > 0 && !p.src.plan && it.pad >= p.tc_min_rows && rec[0] >= kShrinkTcSegMinRank &&
+        rec[0] <= kFuseMaxRank && rec[0] <= p.ld_v)
+        return;                                  // the tensor-core shrink computed this segment
     const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
     const int j0 = blockIdx.y * npc;
     if (j0 >= r) return;
@@ -746,9 +751,10 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
 
 int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
-                       cudaStream_t st, bool skip_fused) {
+                       cudaStream_t st, bool skip_fused, int tc_min_rows) {
     ShrinkParams p;
     p.skip_fused = skip_fused;
+    p.tc_min_rows = tc_min_rows;
     p.pv = pool->view();
     p.src = ItemSource{seg_starts, seg_adapter, S, T, plan,
                        skip_fused && plan ? sgmv_plan_work(pool, matrix, T, const_cast<int *>(plan)) : nullptr};
