@@ -216,6 +216,11 @@ class Runner:
 class DecodeBGMV(Runner):
     name = "decode_bgmv"
 
+    @staticmethod
+    def describe(layers: int = 32) -> str:
+        return ("decode_bgmv: 256 decode tokens, ids ~ U{0..31}, q_proj 4096->4096, rank 16, "
+                f"bf16; step = {layers} layers x lora_bgmv")
+
     def __init__(self, layers: int = 32, seed: int = 0):
         import torch
         from segmented_gathered_rank_gb300 import harness as H
@@ -234,8 +239,7 @@ class DecodeBGMV(Runner):
         self.dominant = dict(name="lora_bgmv (bgmv kernel)", bound="hbm", work_per_launch=per,
                              launches_per_step=layers, unit="GB/s")
         self.working_set = layers * (per + 0)
-        self.config = {"workload": "decode_bgmv: 256 decode tokens, ids ~ U{0..31}, q_proj 4096->4096, rank 16, "
-                                   f"bf16; step = {layers} layers x lora_bgmv",
+        self.config = {"workload": self.describe(layers),
                        "tokens": self.T, "layers": layers, "h_in": self.h, "h_out": self.h, "rank": 16,
                        "adapters": 32, "distinct_adapters": int(len(w.used_adapters())),
                        "l2": f"inputs larger than L2: {layers} layers' x, y and adapter pages "
@@ -279,13 +283,18 @@ class DecodeBGMV(Runner):
             units += self.T
             layers_done += 1
             l += 1
-            if t_total >= budget_s or layers_done >= self.layers * 8:
+            if t_total >= budget_s:
                 break
         return units / t_total, f"{layers_done} layers x {self.T} tokens (oracle.layer, no base), {t_total:.1f} s"
 
 
 class PrefillSGMV(Runner):
     name = "prefill_sgmv"
+
+    @staticmethod
+    def describe(layers: int = 32) -> str:
+        return ("prefill_sgmv: 8192 tokens in 16 Zipf(1.2) segments (cap 2048), 16 of 64 adapters, q/o 4096->4096, "
+                "k/v 4096->1024, rank 16, bf16; step = shrink+expand on q,k,v,o")
 
     def __init__(self, seed: int = 0):
         import torch
@@ -306,9 +315,7 @@ class PrefillSGMV(Runner):
         self.dominant = dict(name="lora_sgmv_expand", bound="hbm", work_per_launch=sum(self.expand_b) / 4,
                              launches_per_step=4, unit="GB/s")
         ws = sum(self.shrink_b) + sum(self.expand_b)
-        self.config = {"workload": "prefill_sgmv: 8192 tokens in 16 Zipf(1.2) segments (cap 2048), 16 of 64 "
-                                   "adapters, q/o 4096->4096, k/v 4096->1024, rank 16, bf16; step = shrink+expand "
-                                   "on q,k,v,o",
+        self.config = {"workload": self.describe(),
                        "tokens": self.T, "segments": w.S, "rank": 16,
                        "l2": f"inputs larger than L2: {ws / 1e6:.0f} MB touched per step"}
 
@@ -361,13 +368,19 @@ class PrefillSGMV(Runner):
             t_total += time.perf_counter() - t0
             units += len(rows)
             n += 1
-            if t_total >= budget_s or n >= 64:
+            if t_total >= budget_s:
                 break
         return units / t_total, f"{n} projections x 1024 sampled tokens (oracle.layer, no base), {t_total:.1f} s"
 
 
 class EncoderMixedRank(Runner):
     name = "encoder_mixed_rank"
+
+    @staticmethod
+    def describe(layers: int = 32) -> str:
+        return ("encoder_mixed_rank: 128 sequences x 128 tokens, Zipf(1.1) ids over 1024 adapters with ranks "
+                "{8,16,32,64} (p .4/.3/.2/.1), 12 layers x q/k/v/o 768->768, pages of 768, bf16; step = "
+                "shrink+expand on 48 projections")
 
     def __init__(self, seed: int = 0):
         import torch
@@ -388,9 +401,7 @@ class EncoderMixedRank(Runner):
         sb = A.shrink_bytes(tok, w.ranks, 768, 2, w.max_rank)
         self.dominant = dict(name="lora_sgmv_expand", bound="hbm", work_per_launch=eb, launches_per_step=self.M,
                              unit="GB/s")
-        self.config = {"workload": "encoder_mixed_rank: 128 sequences x 128 tokens, Zipf(1.1) ids over 1024 "
-                                   "adapters with ranks {8,16,32,64} (p .4/.3/.2/.1), 12 layers x q/k/v/o 768->768, "
-                                   "pages of 768, bf16; step = shrink+expand on 48 projections",
+        self.config = {"workload": self.describe(),
                        "tokens": self.T, "matrices": self.M, "distinct_adapters": len(used),
                        "pool_gb": round(self.pool.n_pages * 768 * 2 / 1e9, 2),
                        "l2": f"inputs larger than L2: {self.M * (eb + sb) / 1e6:.0f} MB touched per step"}
@@ -438,13 +449,18 @@ class EncoderMixedRank(Runner):
             t_total += time.perf_counter() - t0
             units += len(rows)
             n += 1
-            if t_total >= budget_s or n >= 48:
+            if t_total >= budget_s:
                 break
         return units / t_total, f"{n} projections x 2048 sampled tokens (oracle.layer, no base), {t_total:.1f} s"
 
 
 class FusedLayer(Runner):
     name = "fused_layer"
+
+    @staticmethod
+    def describe(layers: int = 32) -> str:
+        return ("fused_layer: 4x1024 prefill + 512 decode tokens, Llama-3-8B q/k/v/o (4096->4096/1024/1024/4096), "
+                "128 adapters Zipf(1.0), rank 16 (adapter 0 rank 128), bf16; step = lora_layer_forward on q,k,v,o")
 
     def __init__(self, seed: int = 0):
         import torch
@@ -465,9 +481,7 @@ class FusedLayer(Runner):
         self.flops = [A.layer_flops(tok, w.ranks, mt.h_in, mt.h_out) for mt in w.matrices]
         self.dominant = dict(name="lora_layer_forward (base GEMM + adapter term)", bound="tensor",
                              work_per_launch=sum(self.flops) / 4, launches_per_step=4, unit="TFLOP/s")
-        self.config = {"workload": "fused_layer: 4x1024 prefill + 512 decode tokens, Llama-3-8B q/k/v/o "
-                                   "(4096->4096/1024/1024/4096), 128 adapters Zipf(1.0), rank 16 (adapter 0 rank "
-                                   "128), bf16; step = lora_layer_forward on q,k,v,o",
+        self.config = {"workload": self.describe(),
                        "tokens": self.T, "flops_per_step": int(sum(self.flops)),
                        "l2": "inputs larger than L2: W 84 MB + x 75 MB + y 94 MB per step"}
 
@@ -512,7 +526,7 @@ class FusedLayer(Runner):
             t_total += time.perf_counter() - t0
             units += len(rows)
             n += 1
-            if t_total >= budget_s or n >= 16:
+            if t_total >= budget_s:
                 break
         return units / t_total, f"{n} projections x 32 sampled tokens (oracle.layer with base), {t_total:.1f} s"
 
@@ -551,7 +565,7 @@ def run_reference(args, dist: Dist):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
+            "config": {"workload": cls.describe(), "tokens": int(r.T)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": samples[-1]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
