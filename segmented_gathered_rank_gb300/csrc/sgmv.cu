@@ -617,14 +617,42 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
             if (bi < nb) issue(bi);
             cp_commit();
         }
-        // v of the item's tokens for this pass, scaled, as two bf16 parts (rows past the item are zero)
-        for (int i = tid; i < kM * kpad; i += kThreadsE) {
-            const int row = i / kpad, j = i % kpad;
-            float val = 0.f;
-            if (row < nt && j < rn) val = scale * p.v[(long long)tok[row] * p.ld_v + j0 + j];
-            const __nv_bfloat16 hi = __float2bfloat16_rn(val);
-            svh[row * vp + j] = hi;
-            svl[row * vp + j] = __float2bfloat16_rn(val - __bfloat162float(hi));
+        // v of the item's tokens for this pass, scaled, as two bf16 parts (rows past the item are
+        // zero).  Groups of 4 ranks; a thread's loads are all issued before any is used.
+        {
+            constexpr int kMaxG = kM * 64 / 4 / kThreadsE;          // groups per thread at kpc = 64
+            const int g4 = kpad >> 2, total = kM * g4;
+            const bool vec = (p.ld_v & 3) == 0;
+            float4 f[kMaxG];
+#pragma unroll
+            for (int u = 0; u < kMaxG; ++u) {
+                const int i = tid + u * kThreadsE, row = i / max(g4, 1), j = 4 * (i % max(g4, 1));
+                f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < total && row < nt && j < rn) {
+                    const float *src = p.v + (long long)tok[row] * p.ld_v + j0 + j;
+                    if (vec) {       // ld_v % 4 == 0 and j0 % 4 == 0: the group stays in the row
+                        f[u] = *reinterpret_cast<const float4 *>(src);
+                    } else {
+                        f[u].x = src[0];
+                        if (j + 1 < rn) f[u].y = src[1];
+                        if (j + 2 < rn) f[u].z = src[2];
+                        if (j + 3 < rn) f[u].w = src[3];
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kMaxG; ++u) {
+                const int i = tid + u * kThreadsE, row = i / max(g4, 1), j = 4 * (i % max(g4, 1));
+                if (i >= total) continue;
+                const float e4[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float val = j + e < rn ? scale * e4[e] : 0.f;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+                    svh[row * vp + j + e] = hi;
+                    svl[row * vp + j + e] = __float2bfloat16_rn(val - __bfloat162float(hi));
+                }
+            }
         }
 
         for (int bi = 0; bi < nb; ++bi) {
