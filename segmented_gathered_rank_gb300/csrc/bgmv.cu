@@ -242,6 +242,10 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
     const int item_idx = blockIdx.x / kC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const PoolView &pv = p.pv;
+    // the next kernel on the stream may start once every CTA of this one has:
+    // its CTAs only read the pool before they wait for this grid to finish,
+    // so their page prefetch overlaps this launch's compute and exchange
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // ---- shared memory carve-up (row pitches padded by 16 B for conflict-free
     //      ldmatrix).  Regions whose lifetimes do not overlap share space: the
@@ -478,7 +482,6 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
             // this CTA's own phase: it expects every CTA's partial (kC x kTok x kJ floats)
             if (tid == 0) mbar_arrive_expect_tx(&bars[0], (uint32_t)(kC * kTok * kJ * sizeof(float)));
         }
-        if (jc == 0) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
         if (!failed && !wait_bar(&bars[0], (uint32_t)jc & 1u)) failed = true;
         if (__syncthreads_or(failed)) {
             if (tid == 0) flag(pv.status, LORA_DEV_WAIT_TIMEOUT);

@@ -368,6 +368,11 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
         const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
         if (((unsigned)it.pad & all) == all) return;
     }
+    // the item's tokens load together with the record (load_record's barrier publishes both)
+    if (tid < kRowsS)
+        tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + row0 + tid] : it.off + row0 + tid, 0),
+                                  p.src.T - 1)
+                            : 0;
     if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0 && blockIdx.z == 0)) return;
     if (p.tc_min_rows > 0 && !p.src.plan && it.pad >= p.tc_min_rows && rec[0] >= kShrinkTcSegMinRank &&
         rec[0] <= kFuseMaxRank && rec[0] <= p.ld_v)
@@ -377,10 +382,6 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
     if (j0 >= r) return;
     const int np = min(npc, r - j0);
     const int npad = (np + 15) & ~15;
-    if (tid < kRowsS)
-        tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + row0 + tid] : it.off + row0 + tid, 0),
-                                  p.src.T - 1)
-                            : 0;
     // rows that never receive copies stay zero
     for (int i = tid; i < kStagesS * kRowsS * (pitch / 8); i += kThreadsS)
         if ((i / (pitch / 8)) % kRowsS >= nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
