@@ -83,18 +83,41 @@ __device__ __forceinline__ uint32_t swz128(int row, int c) {
 // residual), K-major; B2: row n holds B_a[j][n0 + n] (the B rows transposed),
 // K-major.  Every global load of a round is independent of the others but
 // for the page ids, so a round costs about two memory round trips.
+// What round 0 of a tile looks up for every round of it (one thread's share):
+// the adapter's rank and scale and the B page ids of ranks lane + 32 h + 64 rd.
+struct FillCache {
+    int r;
+    float s;
+    int page[2][2];
+};
+
 template <int ST>
 __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t *a2hi, uint8_t *a2lo, uint8_t *b2,
-                            Ctrl<ST> *ctrl, int ethr) {
+                            Ctrl<ST> *ctrl, int ethr, FillCache &fc) {
     const int mb = tile % p.num_m, nb = tile / p.num_m;
-    const int a = p.tile_ad[mb];
-    int r = 0;
-    const int *rec = nullptr;
-    if (a >= 0 && a < p.pv.max_adapters) {
-        rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
-        r = rec[0];
-        if (r < 1 || r > kFuseMaxRank || r > p.ld_v) r = 0;
+    const int lane = ethr & 31, w = ethr >> 5;
+    if (round == 0) {
+        const int a = p.tile_ad[mb];
+        fc.r = 0;
+        fc.s = 0.f;
+        if (a >= 0 && a < p.pv.max_adapters) {
+            const int *rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
+            int r = rec[0];
+            if (r < 1 || r > kFuseMaxRank || r > p.ld_v) r = 0;
+            fc.r = r;
+            if (r > 0) fc.s = __int_as_float(rec[1]);
+            // every round's page ids now: a later round then costs one memory round trip
+#pragma unroll
+            for (int rd = 0; rd < 2; ++rd)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = lane + 32 * h + 64 * rd;
+                    const int pg = j < r ? rec[kRecHeader + r + j] : 0;
+                    fc.page[rd][h] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
+                }
+        }
     }
+    const int r = fc.r;
     const int rounds = (r + 63) / 64;
     const int j0 = round * 64, rn = max(0, min(64, r - j0));
     const int kpad = (rn + 15) & ~15;
@@ -103,16 +126,9 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
         if (round == 0) ctrl->arounds = rounds;
     }
     if (kpad == 0) return rounds;
-    const float s = __int_as_float(rec[1]);
-    const int lane = ethr & 31, w = ethr >> 5;
-    // B page ids of this lane's ranks (lane, lane + 32)
-    int page[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int j = lane + 32 * h;
-        int pg = j < rn ? rec[kRecHeader + r + j0 + j] : 0;
-        page[h] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
-    }
+    const float s = fc.s;
+    // B page ids of this lane's ranks (lane, lane + 32) in this round
+    const int page[2] = {fc.page[round & 1][0], fc.page[round & 1][1]};
     // A2: row ethr of the tile, s * v split into bf16 high part and residual
     {
         const int row = mb * BM + ethr;
@@ -330,6 +346,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // stage every round of a tile's adapter operands, handing each to the MMA warp
         auto stage_tile = [&](int t) {
             int rounds = 1;
+            FillCache fc;
             for (int rd = 0; rd < rounds; ++rd) {
                 if (rd > 0) {
                     const bool okc = wait_phase(&ctrl->aconsumed, n_consumed++ & 1u, abort);
@@ -339,7 +356,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         return;
                     }
                 }
-                rounds = fill_adapter<STAGES>(p, t, rd, a2hi, a2lo, b2, ctrl, ethr);
+                rounds = fill_adapter<STAGES>(p, t, rd, a2hi, a2lo, b2, ctrl, ethr, fc);
                 if (rounds < 1) rounds = 1;
                 fence_proxy_async();
                 __syncwarp();

@@ -180,6 +180,8 @@ RANDOM = [
     dict(seed=5, T=513, h_in=1024, h_out=520, ranks=[8, 64, 16, 32, 1]),
     dict(seed=6, T=129, dtype=I.F32, h_in=96, h_out=128),
     dict(seed=7, T=1000, h_in=4096, h_out=1024, ranks=[16, 128, 16, 4]),
+    # every adapter above rank 64 and segments of 128+ rows: the tensor-core shrink's segment tiles
+    dict(seed=8, T=640, lengths=[512, 0, 127, 1], h_in=512, h_out=256, ranks=[128, 96]),
 ]
 
 
