@@ -243,14 +243,18 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     const int n_items = block_scan<kPlanThreads>(ibase, p.n_ids, wtot);
     int *perm = p.plan + 4;
     Item *items = reinterpret_cast<Item *>(p.plan + 4 + ((p.T + 3) & ~3));
-    for (int a = tid; a < p.n_ids; a += kPlanThreads) {
-        const int n = cnt[a];
-        for (int c = 0; c * kM < n; ++c) {
-            // an invalid (overlapping) segment table can count more than T tokens: never point past T
-            const int off = base[a] + c * kM;
-            const int nt = max(0, min(min(kM, n - c * kM), p.T - off));
-            if (ibase[a] + c < p.max_items) items[ibase[a] + c] = Item{nt > 0 ? a : -1, off, nt, 0};
+    // one thread per item: its adapter is the last whose first item index is <= it
+    for (int i = tid; i < min(n_items, p.max_items); i += kPlanThreads) {
+        int lo = 0, hi = p.n_ids - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ibase[mid] <= i) lo = mid; else hi = mid - 1;
         }
+        const int a = lo, c = i - ibase[a], n = cnt[a];
+        // an invalid (overlapping) segment table can count more than T tokens: never point past T
+        const int off = base[a] + c * kM;
+        const int nt = max(0, min(min(kM, n - c * kM), p.T - off));
+        items[i] = Item{nt > 0 ? a : -1, off, nt, 0};
     }
     if (tid == 0) p.plan[0] = min(n_items, p.max_items);
     for (int i = n_items + tid; i < p.max_items; i += kPlanThreads) items[i] = Item{-1, 0, 0, 0};
@@ -303,24 +307,36 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     }
     __syncthreads();
     // each item's mask of rows that sit in such tiles (the expand skips them;
-    // the item's perm entries are read with independent loads)
-    for (int i = tid; i < min(n_items, p.max_items); i += kPlanThreads) {
-        const Item it = items[i];
-        if (it.a < 0) continue;
-        int tk[kM];
+    // the item's perm entries are read with independent loads); items that keep
+    // other rows go to the work list, one atomic per warp
+    const int nitems = min(n_items, p.max_items);
+    for (int i0 = 0; i0 < nitems; i0 += kPlanThreads) {
+        const int i = i0 + tid;
+        bool want = false;
+        Item w{-1, 0, 0, 0};
+        if (i < nitems) {
+            const Item it = items[i];
+            if (it.a >= 0) {
+                int tk[kM];
 #pragma unroll
-        for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? perm[it.off + k] : -1;
-        unsigned mask = 0;
+                for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? perm[it.off + k] : -1;
+                unsigned mask = 0;
 #pragma unroll
-        for (int k = 0; k < kM; ++k)
-            if (tk[k] >= 0 && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0) mask |= 1u << k;
-        items[i].pad = (int)mask;
-        const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
-        if ((mask & all) != all) {   // rows left for the SGMV kernels (slot order is immaterial)
-            Item w = it;
-            w.pad = (int)mask;
-            p.work[atomicAdd(wcount, 1)] = w;
+                for (int k = 0; k < kM; ++k)
+                    if (tk[k] >= 0 && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0)
+                        mask |= 1u << k;
+                items[i].pad = (int)mask;
+                const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
+                want = (mask & all) != all;        // rows left for the SGMV kernels (slot order is immaterial)
+                w = it;
+                w.pad = (int)mask;
+            }
         }
+        const unsigned bal = __ballot_sync(0xffffffffu, want);
+        int slot = 0;
+        if (lane == 0 && bal) slot = atomicAdd(wcount, __popc(bal));
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+        if (want) p.work[slot + __popc(bal & ((1u << lane) - 1u))] = w;
     }
     __syncthreads();
     if (tid == 0) p.plan[1] = *wcount;
