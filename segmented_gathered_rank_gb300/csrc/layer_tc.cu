@@ -421,10 +421,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 // box, 128-byte swizzle) and warps 2-5 the r page rows of A_a (16-byte
 // cp.async into the same swizzled K-major layout, each thread's copies
 // arriving on the stage's mbarrier as they land); warp 1 issues tcgen05.mma
-// into TMEM.  The splits' partial accumulators then meet in the first CTA of
-// the cluster: the others read theirs out of TMEM and send them with
-// asynchronous remote stores counted on its mbarrier; it adds them, in split
-// order, to its own and stores v.  Rows of a tile past its end (another
+// into TMEM.  The splits' partial accumulators are then reduce-scattered over
+// the cluster: split s owns a quarter of the rank columns, the others read
+// that part of their accumulators out of TMEM and send it with asynchronous
+// remote stores counted on its mbarrier, and it adds the parts in split order
+// and stores its columns of v.  Rows of a tile past its end (another
 // segment's, or past T) are computed and dropped.
 // ---------------------------------------------------------------------------
 constexpr int SK_MAX_STAGES = 8;
@@ -448,8 +449,8 @@ struct SkCtrl {
     uint64_t full[SK_MAX_STAGES];
     uint64_t empty[SK_MAX_STAGES];
     uint64_t done;    // every MMA of the CTA complete
-    uint64_t ready;   // (other splits) the first CTA may receive
-    uint64_t recv;    // (first CTA) every other split's partial has arrived
+    uint64_t ready;   // every other CTA of the cluster may receive
+    uint64_t recv;    // every other split's share of this CTA's columns has arrived
     uint32_t tmem_base;
     int abort;
     int tile[3];      // adapter, first row, rows
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_init(&ctrl->empty[s], 1);
         }
         mbar_init(&ctrl->done, 1);
-        mbar_init(&ctrl->ready, 1);
+        mbar_init(&ctrl->ready, p.nsplit > 1 ? p.nsplit - 1 : 1);   // every other split's ring is drained
         mbar_init(&ctrl->recv, 1);
         ctrl->abort = 0;
         mbar_fence_init();
@@ -701,69 +702,80 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         bool ok = wait_phase(&ctrl->done, 0, nullptr) && !*abort;
         ok = __all_sync(0xffffffffu, ok);
         if (ok) fence_after_sync();
-        const int pitch = npad + 4;                  // floats per received row (16-byte aligned, v4 conflict-free)
-        float *recvbuf = reinterpret_cast<float *>(smem);   // [nsplit - 1][BM][pitch], over the drained ring
-        if (p.nsplit > 1) asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-        if (p.nsplit > 1 && split > 0) {
-            // send this split's partial to the first CTA once it can receive
+        // reduce-scatter over the cluster: split s owns columns [s q, (s + 1) q) of the
+        // partial sums, receives every other split's share of them and writes that part of v
+        const int ns = p.nsplit;
+        const int q = ((npad + ns - 1) / ns + 3) & ~3;   // columns per split (multiple of 4)
+        const int pitch = q + 4;                         // floats per received row (16-byte aligned)
+        auto col_lo = [&](int t) { return min(npad, t * q); };
+        float *recvbuf = reinterpret_cast<float *>(smem);   // [ns][BM][pitch] by sender, over the drained ring
+        const int my_lo = col_lo(split), my_hi = col_lo(split + 1);
+        if (ns > 1) {
+            asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+            // this CTA's ring is drained (all MMAs complete, all copies landed): open it to the others
+            if (threadIdx.x == 64) {
+                mbar_arrive_expect_tx(&ctrl->recv, (uint32_t)((ns - 1) * BM * (my_hi - my_lo) * 4));
+                for (int t = 0; t < ns; ++t)
+                    if (t != split) remote_arrive_sk(&ctrl->ready, t);
+            }
             ok = ok && wait_cluster_sk(&ctrl->ready, 0, abort);
-            if (__all_sync(0xffffffffu, ok)) {
-                const uint32_t rbar = mapa_sk(&ctrl->recv, 0);
-                const uint32_t rdst = mapa_sk(recvbuf + ((long long)(split - 1) * BM + lrow) * pitch, 0);
-                for (int c0 = 0; c0 < npad; c0 += 32) {
-                    float f[32];
-                    __syncwarp();
-                    tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        if (c0 + e < npad) st_async16_sk(rdst + (c0 + e) * 4, rbar, f[e], f[e + 1], f[e + 2], f[e + 3]);
-                }
-            } else if (lane == 0) {
-                flag(p.status, LORA_DEV_WAIT_TIMEOUT);
-            }
-        } else {
-            if (p.nsplit > 1) {
-                // the ring is drained (all MMAs complete, all copies landed): open it to the other splits
-                if (threadIdx.x == 64) {
-                    mbar_arrive_expect_tx(&ctrl->recv, (uint32_t)((p.nsplit - 1) * BM * npad * 4));
-                    for (int s = 1; s < p.nsplit; ++s) remote_arrive_sk(&ctrl->ready, s);
-                }
-                ok = ok && wait_cluster_sk(&ctrl->recv, 0, abort);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok && lane == 0) flag(p.status, LORA_DEV_WAIT_TIMEOUT);
-            }
+            ok = __all_sync(0xffffffffu, ok);
             if (ok) {
-                const int row = row0 + lrow;
-                float *out = p.v + (long long)row * p.ld_v;
-                const bool vec = (p.ld_v & 3) == 0;
-                for (int c0 = 0; c0 < npad; c0 += 32) {
-                    float f[32];
-                    __syncwarp();
-                    tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
-                    for (int s = 1; s < p.nsplit; ++s) {       // split order: deterministic
-                        const float *src = recvbuf + ((long long)(s - 1) * BM + lrow) * pitch + c0;
+                for (int t = 0; t < ns; ++t) {
+                    if (t == split) continue;
+                    const int lo = col_lo(t), hi = col_lo(t + 1);
+                    if (lo >= hi) continue;
+                    const uint32_t rbar = mapa_sk(&ctrl->recv, t);
+                    const uint32_t rdst = mapa_sk(recvbuf + ((long long)split * BM + lrow) * pitch, t);
+                    for (int c0 = lo & ~31; c0 < hi; c0 += 32) {
+                        float f[32];
+                        __syncwarp();
+                        tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), f);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            if (c0 + e < npad) {
-                                const float4 q = *reinterpret_cast<const float4 *>(src + e);
-                                f[e] += q.x;
-                                f[e + 1] += q.y;
-                                f[e + 2] += q.z;
-                                f[e + 3] += q.w;
-                            }
+                        for (int e = 0; e < 32; e += 4)
+                            if (c0 + e >= lo && c0 + e < hi)
+                                st_async16_sk(rdst + (c0 + e - lo) * 4, rbar, f[e], f[e + 1], f[e + 2], f[e + 3]);
+                    }
+                }
+                ok = wait_cluster_sk(&ctrl->recv, 0, abort);
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0) flag(p.status, LORA_DEV_WAIT_TIMEOUT);
+        }
+        if (ok && my_lo < my_hi) {
+            const int row = row0 + lrow;
+            float *out = p.v + (long long)row * p.ld_v;
+            const bool vec = (p.ld_v & 3) == 0;
+            for (int c0 = my_lo & ~31; c0 < my_hi; c0 += 32) {
+                float own[32];
+                __syncwarp();
+                tmem_ld32(tmem + (uint32_t)c0 + ((uint32_t)(sub * 32) << 16), own);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const int col = c0 + e;
+                    if (col < my_lo || col >= my_hi) continue;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int t = 0; t < ns; ++t) {                 // split order: deterministic
+                        float4 f4;
+                        if (t == split) {
+                            f4 = make_float4(own[e], own[e + 1], own[e + 2], own[e + 3]);
+                        } else {
+                            f4 = *reinterpret_cast<const float4 *>(recvbuf + ((long long)t * BM + lrow) * pitch +
+                                                                   (col - my_lo));
                         }
+                        acc.x += f4.x;
+                        acc.y += f4.y;
+                        acc.z += f4.z;
+                        acc.w += f4.w;
                     }
                     if (lrow < rows) {
                         if (vec) {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 4)
-                                if (c0 + e < r)   // r <= ld_v and ld_v % 4 == 0: the float4 stays in the row
-                                    *reinterpret_cast<float4 *>(out + c0 + e) =
-                                        make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+                            if (col < r)   // r <= ld_v and ld_v % 4 == 0: the float4 stays in the row
+                                *reinterpret_cast<float4 *>(out + col) = acc;
                         } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (c0 + e < r) out[c0 + e] = f[e];
+                            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                            for (int u = 0; u < 4; ++u)
+                                if (col + u < r) out[col + u] = a4[u];
                         }
                     }
                 }
@@ -884,7 +896,7 @@ int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x,
     const int npad_max = std::min(kFuseMaxRank, (pool->max_rank + 15) / 16 * 16);
     p.stage_bytes = SK_X_BYTES + npad_max * BK * 2;
     const size_t fixed = sizeof(SkCtrl) + 1024;
-    const size_t need_recv = (size_t)(p.nsplit - 1) * BM * (npad_max + 4) * 4;
+    const size_t need_recv = (size_t)p.nsplit * BM * ((((npad_max + p.nsplit - 1) / p.nsplit + 3) & ~3) + 4) * 4;
     const size_t need_scan = tile_ad ? 0 : (size_t)(S + 1) * 4;
     p.stages = 0;
     for (size_t budget : {(size_t)113 * 1024, (size_t)227 * 1024}) {
