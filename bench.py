@@ -80,13 +80,21 @@ def load_traffic():
 
 
 def source_digest() -> str:
+    """Digest of the kernel sources with comments and blank lines removed, so
+    that counters recorded for a kernel stay attached to it across comment
+    edits and go stale on any change of code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_gathered_rank_gb300", "csrc")
     for n in sorted(os.listdir(csrc)):
         if n.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, n), "rb") as f:
-                h.update(n.encode() + f.read())
+            with open(os.path.join(csrc, n), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", "", text)
+            code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+            h.update(n.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

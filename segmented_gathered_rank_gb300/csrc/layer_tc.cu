@@ -3,18 +3,21 @@
 //   y[t][n] = sum_k x[t][k] W[n][k]
 //
 // "The base part is one big shared matmul for the whole batch"
-// ("Multi-LoRA Serving", section "The kernel trick: gather, do not merge");
-// the per-row low-rank term is added after it by the SGMV expand.
+// ("Multi-LoRA Serving", section "The kernel trick: gather, do not merge").
+// The fused variant also adds the low-rank term s * v . B_a of every M-tile
+// whose 128 rows share one adapter a into the same accumulator (v from the
+// tensor-core shrink below); the other rows get theirs from the SGMV expand.
 //
 // Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles,
 // K in steps of 64.  Warp 0 (one lane) streams x and W tiles into a 4-stage
-// shared-memory ring with TMA (128-byte swizzle); warp 1 (one lane) issues
-// tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of two TMEM
-// accumulators (2 x 256 columns) and commits each ring slot back to the
-// producer and each finished accumulator to the epilogue; warps 2-5 read the
-// accumulator with tcgen05.ld (each warp its 32-lane TMEM sub-partition, one
-// row per thread), round to bf16 and store.  The two accumulators let the epilogue of one tile overlap the
-// main loop of the next.
+// (fused: 3-stage) shared-memory ring with TMA (128-byte swizzle); warp 1
+// (one lane) issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of
+// two TMEM accumulators (2 x 256 columns) and commits each ring slot back to
+// the producer and each finished accumulator to the epilogue; warps 2-5 read
+// the accumulator with tcgen05.ld (each warp its 32-lane TMEM sub-partition,
+// one row per thread), round to bf16 and store, and in the fused variant
+// stage the next uniform tile's s * v and B operands.  The two accumulators
+// let the epilogue of one tile overlap the main loop of the next.
 //
 // Every mbarrier wait is bounded (by the global timer); a wait that gives up
 // sets LORA_DEV_WAIT_TIMEOUT, makes the other roles stop, waits (bounded)
