@@ -356,7 +356,8 @@ struct ShrinkParams {
     int m, h_in;
     bool skip_fused;   // skip plan items whose rows all sit in tensor-core-shrunk tiles
     int tc_min_rows;   // > 0: skip segments of at least this many rows the tensor-core shrink takes
-    int npc;       // ranks per CTA: max_rank rounded up to 16, at most 32 (grid.y covers the rest)
+    int npc;       // ranks per CTA: max_rank rounded up to 16, at most 32 (64 in the wide kernel); grid.y covers the rest
+    int alias_bytes;   // wide kernel: shared bytes of the ring / segment scan / partial sums (they alias)
     const __nv_bfloat16 *x;
     float *v;
     int ld_v;
@@ -498,6 +499,178 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
                 for (int w = 0; w < 3; ++w) {
                     v0 += red[w * 16 * npc + row * npc + j];
                     v1 += red[w * 16 * npc + row * npc + j + 1];
+                }
+                float *vrow = p.v + (long long)tok[row] * p.ld_v + j0;
+                if (j < np) vrow[j] = v0;
+                if (j + 1 < np) vrow[j + 1] = v1;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shrink for pools with ranks above 32: 256 threads, one whole item (up to 32
+// tokens) x one chunk of up to 64 ranks per CTA, so an item's rows share one
+// pass over A_T and a rank-64 adapter needs one chunk.  Warp w takes rows
+// 16 (w & 1) .. +16 and k 32 (w >> 1) .. +32 of every 128-wide stage; the
+// four K-quarter partial sums are added at the end.  The item's x rows are
+// requested before its page-table record arrives.
+// ---------------------------------------------------------------------------
+constexpr int kThreadsW = 256;
+constexpr int kRowsW = kM;
+constexpr int kStagesW = 4;
+
+__global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int pitch = kKs + 8;                                        // bf16 per smem row
+    const int npc = p.npc;
+    __nv_bfloat16 *sx = reinterpret_cast<__nv_bfloat16 *>(smem_raw);     // [stages][32][pitch]
+    __nv_bfloat16 *sa = sx + kStagesW * kRowsW * pitch;                   // [stages][npc][pitch]
+    int *tok = reinterpret_cast<int *>(smem_raw + p.alias_bytes);         // [32]
+    int *wtot = tok + kRowsW;                                            // [kThreadsW / 32 + 4]
+    int *rec = wtot + kThreadsW / 32 + 4;                                // [rec_ints]
+    int *scan = reinterpret_cast<int *>(smem_raw);                       // [S + 1], before the pipeline starts
+    float *red = reinterpret_cast<float *>(smem_raw);                    // [3][32][npc], after it ends
+
+    if (blockIdx.x == 0 && blockIdx.y == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    const Item it = get_item<kThreadsW>(p.src, blockIdx.x, scan, wtot);
+    const int nt = min(kRowsW, it.nt);
+    if (it.a < 0 || nt <= 0) return;
+    if (p.skip_fused && p.src.plan) {
+        const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
+        if (((unsigned)it.pad & all) == all) return;
+    }
+    if (tid < kRowsW)
+        tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
+                            : 0;
+    // x rows past the item stay zero
+    for (int i = tid; i < kStagesW * kRowsW * (pitch / 8); i += kThreadsW)
+        if ((i / (pitch / 8)) % kRowsW >= nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
+    const int nk = p.h_in / kKs;
+    // this thread's 16-byte copy slots, fixed for the whole K loop: element
+    // tid + 256 k of the 32 rows x 16 chunks of x (k < 2) and of the npc (<= 64)
+    // rows x 16 chunks of A_T (k < 4)
+    const __nv_bfloat16 *xs[2], *as[4];
+    uint32_t xd[2], ad[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * kThreadsW, row = i >> 4, kv = i & 15;
+        xs[k] = row < nt ? p.x + (long long)tok[row] * p.h_in + kv * 8 : nullptr;
+        xd[k] = (uint32_t)(row * pitch + kv * 8);
+    }
+    auto issue_x = [&](int kc) {
+        __nv_bfloat16 *dx = sx + (kc % kStagesW) * kRowsW * pitch;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            if (xs[k]) cp_async16(dx + xd[k], xs[k] + kc * kKs);
+    };
+    // x of the first stages is on its way while the page-table record loads
+#pragma unroll
+    for (int kc = 0; kc < kStagesW - 1; ++kc)
+        if (kc < nk) issue_x(kc);
+
+    const bool ok = load_record<kThreadsW>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0);
+    bool skip = !ok;
+    if (ok && p.tc_min_rows > 0 && !p.src.plan && it.pad >= p.tc_min_rows && rec[0] >= kShrinkTcSegMinRank &&
+        rec[0] <= kFuseMaxRank && rec[0] <= p.ld_v)
+        skip = true;                             // the tensor-core shrink computed this segment
+    const int r = ok ? min(rec[0], min(p.pv.max_rank, p.ld_v)) : 0;
+    const int j0 = blockIdx.y * npc;
+    if (skip || j0 >= r) {
+        cp_commit();       // nothing may be in flight into shared memory when the CTA exits
+        cp_wait<0>();
+        return;
+    }
+    const int np = min(npc, r - j0);
+    const int npad = (np + 15) & ~15;
+    // A rows np .. npc-1 receive no copies: zero them in every stage
+    for (int i = tid; i < kStagesW * npc * (pitch / 8); i += kThreadsW)
+        if ((i / (pitch / 8)) % npc >= np) reinterpret_cast<uint4 *>(sa)[i] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + k * kThreadsW, row = i >> 4, kv = i & 15;
+        as[k] = row < np ? page_row<__nv_bfloat16>(p.pv, clamp_page(p.pv, rec[kRecHeader + j0 + row])) + kv * 8 : nullptr;
+        ad[k] = (uint32_t)(row * pitch + kv * 8);
+    }
+    auto issue_a = [&](int kc) {
+        __nv_bfloat16 *da = sa + (kc % kStagesW) * npc * pitch;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (as[k]) cp_async16(da + ad[k], as[k] + kc * kKs);
+    };
+#pragma unroll
+    for (int kc = 0; kc < kStagesW - 1; ++kc)
+        if (kc < nk) issue_a(kc);
+    cp_commit();            // one group holds stages 0 .. kStagesW-2
+
+    const int mh = warp & 1, kq = warp >> 1;
+    const int g = lane >> 2, q = lane & 3;
+    float d[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+    for (int kc = 0; kc < nk; ++kc) {
+        if (kc == 0) cp_wait<0>();
+        else cp_wait<kStagesW - 2>();
+        __syncthreads();
+        if (kc + kStagesW - 1 < nk) {
+            issue_x(kc + kStagesW - 1);
+            issue_a(kc + kStagesW - 1);
+        }
+        cp_commit();
+        const int st = kc % kStagesW;
+        const __nv_bfloat16 *bx = sx + st * kRowsW * pitch;
+        const __nv_bfloat16 *ba = sa + st * npc * pitch;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {                   // this warp's quarter of the stage
+            const int k = kq * 32 + ks * 16;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(bx + (mh * 16 + (lane & 15)) * pitch + k + (lane >> 4) * 8, a0, a1, a2, a3);
+#pragma unroll
+            for (int t = 0; t < 8; t += 2) {
+                if (t * 8 >= npad) break;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(ba + (t * 8 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k + ((lane >> 3) & 1) * 8, b0, b1,
+                        b2, b3);
+                mma16816(d[t], a0, a1, a2, a3, b0, b1);
+                mma16816(d[t + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+    }
+    cp_wait<0>();
+    __syncthreads();        // the pipeline buffers are free: red aliases them
+    // add the four K-quarter partials and write v
+    if (kq > 0) {
+        float *rw = red + (kq - 1) * kRowsW * npc;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (t * 8 >= npad) break;
+            const int r0 = mh * 16 + g;
+            rw[r0 * npc + t * 8 + 2 * q] = d[t][0];
+            rw[r0 * npc + t * 8 + 2 * q + 1] = d[t][1];
+            rw[(r0 + 8) * npc + t * 8 + 2 * q] = d[t][2];
+            rw[(r0 + 8) * npc + t * 8 + 2 * q + 1] = d[t][3];
+        }
+    }
+    __syncthreads();
+    if (kq == 0) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (t * 8 >= npad) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = mh * 16 + g + 8 * h;
+                const int j = t * 8 + 2 * q;
+                if (row >= nt) continue;
+                float v0 = d[t][2 * h], v1 = d[t][2 * h + 1];
+#pragma unroll
+                for (int w = 0; w < 3; ++w) {
+                    v0 += red[w * kRowsW * npc + row * npc + j];
+                    v1 += red[w * kRowsW * npc + row * npc + j + 1];
                 }
                 float *vrow = p.v + (long long)tok[row] * p.ld_v + j0;
                 if (j < np) vrow[j] = v0;
@@ -805,10 +978,33 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
                        skip_fused && plan ? sgmv_plan_work(pool, matrix, T, const_cast<int *>(plan)) : nullptr};
     p.m = matrix;
     p.h_in = h_in;
-    p.npc = std::min(32, (pool->max_rank + 15) / 16 * 16);
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.v = v;
     p.ld_v = ld_v;
+    const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
+    if (pool->max_rank > 32 && !plan) {
+        // ranks above 32 in a segment table: whole items and 64-rank chunks per CTA
+        p.npc = std::min(64, (pool->max_rank + 15) / 16 * 16);
+        constexpr int pitch = kKs + 8;
+        const size_t pipe = (size_t)kStagesW * (kRowsW + p.npc) * pitch * 2;
+        const size_t alias = (std::max({pipe, (size_t)3 * kRowsW * p.npc * 4, (size_t)(S + 1) * 4}) + 15) &
+                             ~(size_t)15;
+        p.alias_bytes = (int)alias;
+        const size_t smem_w = alias + (size_t)(kRowsW + kThreadsW / 32 + 4 + p.pv.rec_ints) * 4;
+        static size_t configured_w = 0;
+        if (smem_w > configured_w) {
+            if (cudaFuncSetAttribute(sgmv_shrink_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_w) != cudaSuccess)
+                return LORA_ERR_CUDA;
+            configured_w = smem_w;
+        }
+        const dim3 grid_w(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc, 1);
+        sgmv_shrink_wide_kernel<<<grid_w, kThreadsW, smem_w, st>>>(p);
+        count_launch();
+        return cuda_status(cudaGetLastError());
+    }
+    p.npc = std::min(32, (pool->max_rank + 15) / 16 * 16);
+    p.alias_bytes = 0;
     const size_t smem = (size_t)kStagesS * (kRowsS + p.npc) * (kKs + 8) * 2 + (size_t)3 * 16 * p.npc * 4 +
                         (size_t)(kRowsS + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
     static size_t configured = 0;
@@ -818,7 +1014,6 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
             return LORA_ERR_CUDA;
         configured = smem;
     }
-    const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
     const dim3 grid(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc, kM / kRowsS);
     sgmv_shrink_kernel<<<grid, kThreadsS, smem, st>>>(p);
     count_launch();
