@@ -218,7 +218,8 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
                        cudaStream_t st, const int *tile_ad = nullptr);
 // Groups a batch's tokens by adapter into kM-token items (counting sort).
-bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S);
+// units: the plan also lists the persistent shrink / expand units (layer plans with GEMM-fused tiles)
+bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S, int T, bool units);
 size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T);
 // The plan's per-M-tile array (after its items).
 int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan);

@@ -67,6 +67,33 @@ __global__ void set_rank_kernel(int *table, long long rec_off, int rank) { table
 }  // namespace lora
 
 namespace lora {
+// A second stream, per host thread and device, for the part of a layer call
+// that may run beside the main stream's kernels, with the events that fork it
+// from the main stream and join it back.  Under stream capture the fork and
+// join become graph edges.
+struct SideStream {
+    int device = -1;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream *side_stream() {
+    thread_local SideStream ss;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (ss.device != dev) {
+        // a stream of another device stays as it is: work of this thread may still use it
+        SideStream n;
+        if (cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+        n.device = dev;
+        ss = n;
+    }
+    return &ss;
+}
+
 // The adapted layer given scratch for v (T x max_rank fp32): base product for
 // the whole batch (tensor cores when the shape allows), then each token's own
 // low-rank term: shrink into v, expand into y.
@@ -74,24 +101,38 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
                        const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st) {
     int rc;
     const bool tc = gemm_tc_ok(p, h_in, h_out, T);
-    if (sgmv_plan_ok(p, matrix, S) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
+    const bool tcs = tc && shrink_tc_ok(p, h_in, S);
+    if (sgmv_plan_ok(p, matrix, S, T, tcs) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
         // 1. plan: tokens grouped by adapter; GEMM M-tiles whose rows share one adapter
         // 2. (tensor cores) v of those tiles: M 128 x N r contractions, K split over a cluster
         // 3. v of every other adapted token (warp-MMA SGMV shrink)
         // 4. base product; the uniform tiles add their low-rank term inside the GEMM
         // 5. expand the remaining rows
+        // With tensor-core tiles, 3 reads only the plan and x and writes only v rows outside
+        // those tiles, which 2 and 4 never touch: it runs on a side stream beside them and
+        // joins before 5.
         int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
                                             ~uintptr_t(255));
-        const bool tcs = tc && shrink_tc_ok(p, h_in, S);
         int *tile_ad = tcs ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
         if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, tile_ad))) return rc;
+        SideStream *side = tcs ? side_stream() : nullptr;
+        if (side && cudaEventRecord(side->fork, st) != cudaSuccess) return LORA_ERR_CUDA;
         if (tcs && (rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, nullptr, nullptr, 0, v, p->max_rank, st)))
             return rc;
-        if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st,
-                                     tcs)))
+        cudaStream_t st3 = st;
+        if (side) {
+            if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return LORA_ERR_CUDA;
+            st3 = side->s;
+        }
+        rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st3, tcs);
+        if (side && cudaEventRecord(side->join, side->s) != cudaSuccess) return LORA_ERR_CUDA;
+        if (rc) {
+            if (side) cudaStreamWaitEvent(st, side->join, 0);     // no side work is left unjoined
             return rc;
+        }
         rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank)
                 : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+        if (side && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return LORA_ERR_CUDA;
         if (rc) return rc;
         return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st,
                                   tile_ad);

@@ -19,6 +19,8 @@
 // tokens by at most a few dozen ranks, and the kernels are bound by HBM
 // traffic, not MMA rate.  In the expand, v enters the MMA as a bf16 high part
 // plus a bf16 residual, which keeps the product within fp32-level error.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 
 #include "internal.cuh"
@@ -26,9 +28,12 @@
 namespace lora {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kM = 32;            // tokens per item (one per lane where a warp collects an item's tokens)
 static_assert(kM == 32, "an item's tokens are collected one per lane of a warp");
 constexpr int kKs = 128;          // k per shrink pipeline stage
+constexpr int kRowsS = 16;        // rows per 128-thread shrink CTA (half an item)
 constexpr int kStagesS = 4;
 constexpr int kNb = 128;          // output columns per expand block
 constexpr int kMaxBlocksPerUnit = 8; // column blocks per expand unit (up to 1024 columns)
@@ -87,14 +92,16 @@ __device__ int block_scan(int *v, int n, int *wtot) {
     }
     if (lane == 31) wtot[warp] = inc;
     __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int w = 0; w < NW; ++w) {
-            const int t = wtot[w];
-            wtot[w] = run;
-            run += t;
+    if (warp == 0) {      // exclusive scan of the warp totals (NW <= 32)
+        const int t = lane < NW ? wtot[lane] : 0;
+        int run = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run += u;
         }
-        wtot[NW] = run;
+        if (lane < NW) wtot[lane] = run - t;
+        if (lane == NW - 1) wtot[NW] = run;
     }
     __syncthreads();
     int run = wtot[warp] + inc - sum;
@@ -108,6 +115,52 @@ __device__ int block_scan(int *v, int n, int *wtot) {
     return total;
 }
 
+__device__ __forceinline__ int4 add4(int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+
+// Exclusive scan of four counts per element (v[0..n)) in place; returns the four totals.
+// wtot: NT/32 + 1 int4 of shared memory.
+template <int NT>
+__device__ int4 block_scan4(int4 *v, int n, int4 *wtot) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + NT - 1) / NT;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int4 sum = make_int4(0, 0, 0, 0);
+    for (int i = lo; i < hi; ++i) sum = add4(sum, v[i]);
+    int4 inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int4 t = make_int4(__shfl_up_sync(0xffffffffu, inc.x, o), __shfl_up_sync(0xffffffffu, inc.y, o),
+                                 __shfl_up_sync(0xffffffffu, inc.z, o), __shfl_up_sync(0xffffffffu, inc.w, o));
+        if (lane >= o) inc = add4(inc, t);
+    }
+    if (lane == 31) wtot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {      // exclusive scan of the warp totals (NW <= 32)
+        const int4 t = lane < NW ? wtot[lane] : make_int4(0, 0, 0, 0);
+        int4 run = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int4 u = make_int4(__shfl_up_sync(0xffffffffu, run.x, o), __shfl_up_sync(0xffffffffu, run.y, o),
+                                     __shfl_up_sync(0xffffffffu, run.z, o), __shfl_up_sync(0xffffffffu, run.w, o));
+            if (lane >= o) run = add4(run, u);
+        }
+        if (lane < NW) wtot[lane] = make_int4(run.x - t.x, run.y - t.y, run.z - t.z, run.w - t.w);
+        if (lane == NW - 1) wtot[NW] = run;
+    }
+    __syncthreads();
+    int4 run = wtot[warp];
+    run = make_int4(run.x + inc.x - sum.x, run.y + inc.y - sum.y, run.z + inc.z - sum.z, run.w + inc.w - sum.w);
+    for (int i = lo; i < hi; ++i) {
+        const int4 t = v[i];
+        v[i] = run;
+        run = add4(run, t);
+    }
+    const int4 total = wtot[NW];
+    __syncthreads();
+    return total;
+}
+
 // An item: adapter `a` and its tokens; row i of the item is token
 // perm ? perm[off + i] : off + i.
 struct Item {
@@ -115,6 +168,17 @@ struct Item {
     int off;
     int nt;
     int pad;    // plan with GEMM-fused tiles: bit k set when row k's term is added by the GEMM
+};
+
+// A unit of the persistent shrink and expand kernels of a layer plan: one
+// work item's rows with one rank chunk (shrink) or a range of column blocks
+// (expand).  The plan lists the costly units first.
+struct Unit {
+    int a;
+    int off;
+    int info;   // bits 0-5: the item's token count; shrink: bit 6 the 16-row half, bits 8+ the rank
+                // chunk; expand: bits 6-9 the unit's column blocks, bits 10+ its first column block
+    int pad;    // the item's mask of rows whose term the GEMM adds
 };
 
 // Item `idx` among the (segment, kM-token chunk) pairs of a segment table.
@@ -206,17 +270,35 @@ struct PlanParams {
     int *tile_ad;       // nullptr, or [n_tiles]: adapter whose term the GEMM adds for that M-tile, -1 if none
     int n_tiles;
     Item *work;         // with tile_ad: compacted copies of the items that keep rows outside such tiles
+    Unit *su, *eu;      // with tile_ad: shrink and expand units of the work items (counts plan[2], plan[3])
+    int npc_s;          // ranks per shrink unit
+    int nb_total;       // column blocks of kNb in h_out
+    int bpu;            // column blocks per expand unit of cheap items
+    int rank_cap;       // ranks beyond this are not computed (the v row length)
+    int body;           // ints of the counting-sort area of shared memory
 };
 
+// Column blocks per expand unit from an item's cost per block: its y rows,
+// read and written once per pass of up to 64 ranks, plus its B rows.
+__device__ __forceinline__ int expand_bpu(int nt, int r, int bpu_cheap) {
+    const int cost = 2 * nt * ((r + 63) / 64) + r;
+    return cost >= 48 ? 1 : (cost >= 24 ? 2 : bpu_cheap);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
-    extern __shared__ int sm[];
+    extern __shared__ __align__(16) int sm[];
     int *cnt = sm;                       // [n_ids] tokens per adapter
     int *base = cnt + p.n_ids;           // [n_ids] token offset of each adapter
     int *ibase = base + p.n_ids;         // [n_ids] item offset of each adapter
     int *segoff = ibase + p.n_ids;       // [S] offset of each segment within its adapter's tokens
     int *sb = segoff + p.S;              // [S + 1] segment bounds, clamped into [0, T]
     int *sa = sb + p.S + 1;              // [S] segment adapters (-1: none or invalid)
-    int *wtot = sa + p.S;                // [kPlanThreads / 32 + 1]
+    int *wtot = sm + p.body;             // [kPlanThreads / 32 + 1], then the work count
+    // with units: [max_items] int4 work items, int4 unit counts and ranks, after the counters
+    int4 *sitem = reinterpret_cast<int4 *>(sm + p.body + ((kPlanThreads / 32 + 2 + 3) & ~3));
+    int4 *ucnt = sitem + p.max_items;
+    int4 *wtot4 = ucnt + p.max_items;    // [kPlanThreads / 32 + 1]
+    int *srank = reinterpret_cast<int *>(wtot4 + kPlanThreads / 32 + 1);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = kPlanThreads / 32;
     check_segments(p.seg_starts, p.S, p.T, p.status);
@@ -314,9 +396,11 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         const int i = i0 + tid;
         bool want = false;
         Item w{-1, 0, 0, 0};
+        int rank = 0;
         if (i < nitems) {
             const Item it = items[i];
             if (it.a >= 0) {
+                if (p.su) rank = p.pv.table[((long long)it.a * p.pv.n_matrices + p.m) * p.pv.rec_ints];
                 int tk[kM];
 #pragma unroll
                 for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? perm[it.off + k] : -1;
@@ -336,19 +420,69 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         int slot = 0;
         if (lane == 0 && bal) slot = atomicAdd(wcount, __popc(bal));
         slot = __shfl_sync(0xffffffffu, slot, 0);
-        if (want) p.work[slot + __popc(bal & ((1u << lane) - 1u))] = w;
+        if (want) {
+            const int k = slot + __popc(bal & ((1u << lane) - 1u));
+            p.work[k] = w;
+            if (p.su) {
+                // units of this item: 16-row halves that keep rows x rank chunks (shrink), column
+                // block ranges (expand); counted in the costly class or the cheap one
+                if (rank < 0) flag(p.status, LORA_DEV_BAD_ADAPTER);
+                const int r = min(rank, p.rank_cap);
+                int4 c = make_int4(0, 0, 0, 0);
+                if (r > 0) {
+                    const unsigned all = w.nt >= 32 ? 0xffffffffu : ((1u << w.nt) - 1u);
+                    const unsigned left = ~(unsigned)w.pad & all;
+                    const int nh = ((left & 0xffffu) != 0u) + ((left >> 16) != 0u);
+                    const int nch = (r + p.npc_s - 1) / p.npc_s;
+                    const int bpu = expand_bpu(w.nt, r, p.bpu);
+                    const int ne = (p.nb_total + bpu - 1) / bpu;
+                    const bool costly_s = min(w.nt, kRowsS) + min(r, p.npc_s) >= 32;
+                    c = make_int4(costly_s ? nh * nch : 0, costly_s ? 0 : nh * nch, bpu == 1 ? ne : 0,
+                                  bpu == 1 ? 0 : ne);
+                }
+                sitem[k] = make_int4(w.a, w.off, w.nt, w.pad);
+                ucnt[k] = c;
+                srank[k] = max(r, 0);
+            }
+        }
     }
     __syncthreads();
-    if (tid == 0) p.plan[1] = *wcount;
+    const int n_work = *wcount;
+    if (tid == 0) p.plan[1] = n_work;
+    if (!p.su) return;
+    const int4 tot = block_scan4<kPlanThreads>(ucnt, n_work, wtot4);
+    for (int k = tid; k < n_work; k += kPlanThreads) {
+        const int r = srank[k];
+        if (r <= 0) continue;
+        const int4 w = sitem[k], c = ucnt[k];
+        const unsigned all = w.z >= 32 ? 0xffffffffu : ((1u << w.z) - 1u);
+        const unsigned left = ~(unsigned)w.w & all;
+        const int nch = (r + p.npc_s - 1) / p.npc_s;
+        const bool costly_s = min(w.z, kRowsS) + min(r, p.npc_s) >= 32;
+        int u = costly_s ? c.x : tot.x + c.y;
+        for (int h = 0; h < 2; ++h) {
+            if (!((left >> (16 * h)) & 0xffffu)) continue;
+            for (int ch = 0; ch < nch; ++ch) p.su[u++] = Unit{w.x, w.y, w.z | (h << 6) | (ch << 8), w.w};
+        }
+        const int bpu = expand_bpu(w.z, r, p.bpu);
+        u = bpu == 1 ? c.z : tot.z + c.w;
+        for (int b = 0; b < p.nb_total; b += bpu)
+            p.eu[u++] = Unit{w.x, w.y, w.z | (min(bpu, p.nb_total - b) << 6) | (b << 10), w.w};
+    }
+    if (tid == 0) {
+        p.plan[2] = tot.x + tot.y;
+        p.plan[3] = tot.z + tot.w;
+    }
 }
 
 // ---------------------------------------------------------------------------
-// Shrink: 128 threads, one half (16 tokens, grid.z) of an item x one chunk of
-// npc ranks (grid.y); K in 128-wide stages, warp w takes k 32w .. 32w+31 of
-// every stage and the four partial sums are added at the end.
+// Shrink: 128 threads, one half (16 tokens) of an item x one chunk of npc
+// ranks; K in 128-wide stages, warp w takes k 32w .. 32w+31 of every stage and
+// the four partial sums are added at the end.  Two kernels share the core:
+// one CTA per (item, chunk, half) from the grid, or (layer plans) persistent
+// clusters that walk the plan's unit list and split K over the cluster's CTAs.
 // ---------------------------------------------------------------------------
 constexpr int kThreadsS = 128;
-constexpr int kRowsS = 16;
 
 struct ShrinkParams {
     PoolView pv;
@@ -361,7 +495,122 @@ struct ShrinkParams {
     const __nv_bfloat16 *x;
     float *v;
     int ld_v;
+    const Unit *units;   // unit kernel: the plan's shrink units (count plan[2])
 };
+
+// Rows tok[0 .. nt) of x, K stages kc0 .. kc1-1, times ranks j0 .. j0+np-1 of the
+// adapter whose record is in rec.  On return warp 0's d holds the CTA's sums
+// (fragment rows g and g + 8, rank pairs t * 8 + 2q); the other warps' d are spent.
+__device__ __forceinline__ void shrink_core(const ShrinkParams &p, const int *tok, int nt, const int *rec, int j0,
+                                            int np, int kc0, int kc1, __nv_bfloat16 *sx, __nv_bfloat16 *sa,
+                                            float *red, float (&d)[4][4]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int pitch = kKs + 8;                                        // bf16 per smem row
+    const int npc = p.npc;
+    const int npad = (np + 15) & ~15;
+    // rows that never receive copies stay zero
+    for (int i = tid; i < kStagesS * kRowsS * (pitch / 8); i += kThreadsS)
+        if ((i / (pitch / 8)) % kRowsS >= nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < kStagesS * npc * (pitch / 8); i += kThreadsS)
+        if ((i / (pitch / 8)) % npc >= np) reinterpret_cast<uint4 *>(sa)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
+    const int g = lane >> 2, q = lane & 3;
+    const int nk = kc1 - kc0;
+    // this thread's 16-byte copy slots, fixed for the whole K loop: element
+    // tid + 128 k of the 16 rows x 16 chunks of x (k < 2) and of the npc rows
+    // x 16 chunks of A_T (k < 4)
+    const __nv_bfloat16 *xs[2], *as[4];
+    uint32_t xd[2], ad[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * kThreadsS, row = i >> 4, kv = i & 15;
+        xs[k] = row < nt ? p.x + (long long)tok[row] * p.h_in + kc0 * kKs + kv * 8 : nullptr;
+        xd[k] = (uint32_t)(row * pitch + kv * 8);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + k * kThreadsS, row = i >> 4, kv = i & 15;
+        as[k] = row < np ? page_row<__nv_bfloat16>(p.pv, clamp_page(p.pv, rec[kRecHeader + j0 + row])) + kc0 * kKs +
+                               kv * 8
+                         : nullptr;
+        ad[k] = (uint32_t)(row * pitch + kv * 8);
+    }
+    auto issue = [&](int kc) {
+        const int st = kc % kStagesS;
+        __nv_bfloat16 *dx = sx + st * kRowsS * pitch;
+        __nv_bfloat16 *da = sa + st * npc * pitch;
+        const int ko = kc * kKs;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            if (xs[k]) cp_async16(dx + xd[k], xs[k] + ko);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (as[k]) cp_async16(da + ad[k], as[k] + ko);
+    };
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < kStagesS - 1; ++kc) {
+        if (kc < nk) issue(kc);
+        cp_commit();
+    }
+    for (int kc = 0; kc < nk; ++kc) {
+        cp_wait<kStagesS - 2>();
+        __syncthreads();
+        if (kc + kStagesS - 1 < nk) issue(kc + kStagesS - 1);
+        cp_commit();
+        const int st = kc % kStagesS;
+        const __nv_bfloat16 *bx = sx + st * kRowsS * pitch;
+        const __nv_bfloat16 *ba = sa + st * npc * pitch;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {                   // this warp's quarter of the stage
+            const int k = warp * 32 + ks * 16;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(bx + (lane & 15) * pitch + k + (lane >> 4) * 8, a0, a1, a2, a3);
+#pragma unroll
+            for (int t = 0; t < 4; t += 2) {
+                if (t * 8 >= npad) break;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(ba + (t * 8 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k + ((lane >> 3) & 1) * 8, b0, b1,
+                        b2, b3);
+                mma16816(d[t], a0, a1, a2, a3, b0, b1);
+                mma16816(d[t + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+    }
+    cp_wait<0>();
+    // add the four k-quarter partials into warp 0's fragment
+    if (warp > 0) {
+        float *rw = red + (warp - 1) * 16 * npc;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (t * 8 >= npad) break;
+            rw[g * npc + t * 8 + 2 * q] = d[t][0];
+            rw[g * npc + t * 8 + 2 * q + 1] = d[t][1];
+            rw[(g + 8) * npc + t * 8 + 2 * q] = d[t][2];
+            rw[(g + 8) * npc + t * 8 + 2 * q + 1] = d[t][3];
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (t * 8 >= npad) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = g + 8 * h, j = t * 8 + 2 * q;
+#pragma unroll
+                for (int w = 0; w < 3; ++w) {
+                    d[t][2 * h] += red[w * 16 * npc + row * npc + j];
+                    d[t][2 * h + 1] += red[w * 16 * npc + row * npc + j + 1];
+                }
+            }
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -398,113 +647,88 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
     const int j0 = blockIdx.y * npc;
     if (j0 >= r) return;
     const int np = min(npc, r - j0);
-    const int npad = (np + 15) & ~15;
-    // rows that never receive copies stay zero
-    for (int i = tid; i < kStagesS * kRowsS * (pitch / 8); i += kThreadsS)
-        if ((i / (pitch / 8)) % kRowsS >= nt) reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < kStagesS * npc * (pitch / 8); i += kThreadsS)
-        if ((i / (pitch / 8)) % npc >= np) reinterpret_cast<uint4 *>(sa)[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-
-    const int g = lane >> 2, q = lane & 3;
-    const int nk = p.h_in / kKs;
-    // this thread's 16-byte copy slots, fixed for the whole K loop: element
-    // tid + 128 k of the 16 rows x 16 chunks of x (k < 2) and of the npc rows
-    // x 16 chunks of A_T (k < 4)
-    const __nv_bfloat16 *xs[2], *as[4];
-    uint32_t xd[2], ad[4];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int i = tid + k * kThreadsS, row = i >> 4, kv = i & 15;
-        xs[k] = row < nt ? p.x + (long long)tok[row] * p.h_in + kv * 8 : nullptr;
-        xd[k] = (uint32_t)(row * pitch + kv * 8);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int i = tid + k * kThreadsS, row = i >> 4, kv = i & 15;
-        as[k] = row < np ? page_row<__nv_bfloat16>(p.pv, clamp_page(p.pv, rec[kRecHeader + j0 + row])) + kv * 8 : nullptr;
-        ad[k] = (uint32_t)(row * pitch + kv * 8);
-    }
-    auto issue = [&](int kc) {
-        const int st = kc % kStagesS;
-        __nv_bfloat16 *dx = sx + st * kRowsS * pitch;
-        __nv_bfloat16 *da = sa + st * npc * pitch;
-        const int ko = kc * kKs;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-            if (xs[k]) cp_async16(dx + xd[k], xs[k] + ko);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (as[k]) cp_async16(da + ad[k], as[k] + ko);
-    };
     float d[4][4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
-#pragma unroll
-    for (int kc = 0; kc < kStagesS - 1; ++kc) {
-        if (kc < nk) issue(kc);
-        cp_commit();
-    }
-    for (int kc = 0; kc < nk; ++kc) {
-        cp_wait<kStagesS - 2>();
-        __syncthreads();
-        if (kc + kStagesS - 1 < nk) issue(kc + kStagesS - 1);
-        cp_commit();
-        const int st = kc % kStagesS;
-        const __nv_bfloat16 *bx = sx + st * kRowsS * pitch;
-        const __nv_bfloat16 *ba = sa + st * npc * pitch;
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {                   // this warp's quarter of the stage
-            const int k = warp * 32 + ks * 16;
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(bx + (lane & 15) * pitch + k + (lane >> 4) * 8, a0, a1, a2, a3);
-#pragma unroll
-            for (int t = 0; t < 4; t += 2) {
-                if (t * 8 >= npad) break;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(ba + (t * 8 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k + ((lane >> 3) & 1) * 8, b0, b1,
-                        b2, b3);
-                mma16816(d[t], a0, a1, a2, a3, b0, b1);
-                mma16816(d[t + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-    }
-    cp_wait<0>();
-    // add the four k-quarter partials and write v
-    if (warp > 0) {
-        float *rw = red + (warp - 1) * 16 * npc;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            if (t * 8 >= npad) break;
-            rw[g * npc + t * 8 + 2 * q] = d[t][0];
-            rw[g * npc + t * 8 + 2 * q + 1] = d[t][1];
-            rw[(g + 8) * npc + t * 8 + 2 * q] = d[t][2];
-            rw[(g + 8) * npc + t * 8 + 2 * q + 1] = d[t][3];
-        }
-    }
-    __syncthreads();
+    shrink_core(p, tok, nt, rec, j0, np, 0, p.h_in / kKs, sx, sa, red, d);
     if (warp == 0) {
+        const int g = lane >> 2, q = lane & 3;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            if (t * 8 >= npad) break;
+            if (t * 8 >= np) break;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int row = g + 8 * h;
-                const int j = t * 8 + 2 * q;
+                const int row = g + 8 * h, j = t * 8 + 2 * q;
                 if (row >= nt) continue;
-                float v0 = d[t][2 * h], v1 = d[t][2 * h + 1];
-#pragma unroll
-                for (int w = 0; w < 3; ++w) {
-                    v0 += red[w * 16 * npc + row * npc + j];
-                    v1 += red[w * 16 * npc + row * npc + j + 1];
-                }
                 float *vrow = p.v + (long long)tok[row] * p.ld_v + j0;
-                if (j < np) vrow[j] = v0;
-                if (j + 1 < np) vrow[j + 1] = v1;
+                if (j < np) vrow[j] = d[t][2 * h];
+                if (j + 1 < np) vrow[j + 1] = d[t][2 * h + 1];
             }
         }
+    }
+}
+
+// Layer plans: each cluster of ks CTAs (grid (ks, clusters)) walks the plan's
+// shrink units, CTA c of the cluster taking the c-th of ks equal K ranges.  The
+// ks partial sums meet in distributed shared memory; CTA c adds, in cluster
+// rank order, the rows congruent to c mod ks and writes them to v.  Rows whose
+// tile the tensor-core shrink covers keep that kernel's v.
+__global__ void __launch_bounds__(kThreadsS, 3) sgmv_shrink_units_kernel(ShrinkParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int pitch = kKs + 8;
+    const int npc = p.npc;
+    __nv_bfloat16 *sx = reinterpret_cast<__nv_bfloat16 *>(smem_raw);     // [stages][16][pitch]
+    __nv_bfloat16 *sa = sx + kStagesS * kRowsS * pitch;                  // [stages][npc][pitch]
+    float *red = reinterpret_cast<float *>(sa + kStagesS * npc * pitch);  // [3][16][npc] partials of warps 1..3
+    float *part = red + 3 * 16 * npc;                                    // [16][npc] this CTA's sums
+    int *tok = reinterpret_cast<int *>(part + 16 * npc);                 // [16]
+    int *rec = tok + kRowsS;                                             // [rec_ints]
+
+    cg::cluster_group cl = cg::this_cluster();
+    const int ks = (int)cl.num_blocks(), kpart = (int)cl.block_rank();
+    const int n_units = p.src.plan[2];
+    const int G = gridDim.y, c = blockIdx.y;
+    const int nk = p.h_in / kKs;
+    const int kc0 = kpart * nk / ks, kc1 = (kpart + 1) * nk / ks;
+    const int g = lane >> 2, q = lane & 3;
+    for (int k = 0;; ++k) {
+        // snake order over the cost-sorted list: cluster c takes units c, 2G - 1 - c, 2G + c, ...
+        const int u = k * G + ((k & 1) ? G - 1 - c : c);
+        if (u >= n_units) break;                  // the same for every CTA of the cluster
+        const Unit un = p.units[u];
+        const int row0 = ((un.info >> 6) & 1) * kRowsS, chunk = un.info >> 8;
+        const int nt = min(kRowsS, (un.info & 63) - row0);
+        __syncthreads();                          // the previous unit's readers of tok and rec are done
+        if (tid < kRowsS)
+            tok[tid] = tid < nt ? min(max(plan_perm(p.src.plan)[un.off + row0 + tid], 0), p.src.T - 1) : 0;
+        if (!load_record<kThreadsS>(p.pv, un.a, p.m, rec, false)) continue;
+        const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
+        const int j0 = chunk * npc;
+        if (j0 >= r || nt <= 0) continue;
+        const int np = min(npc, r - j0);
+        float d[4][4];
+        shrink_core(p, tok, nt, rec, j0, np, kc0, kc1, sx, sa, red, d);
+        if (warp == 0) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                if (t * 8 >= np) break;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = g + 8 * h, j = t * 8 + 2 * q;
+                    part[row * npc + j] = d[t][2 * h];
+                    part[row * npc + j + 1] = d[t][2 * h + 1];
+                }
+            }
+        }
+        cl.sync();                                // every CTA's part is written
+        const int own = nt > kpart ? (nt - 1 - kpart) / ks + 1 : 0;
+        for (int i = tid; i < own * np; i += kThreadsS) {
+            const int row = kpart + (i / np) * ks, j = i % np;
+            if (((unsigned)un.pad >> (row0 + row)) & 1u) continue;
+            float sum = 0.f;
+            for (int qq = 0; qq < ks; ++qq) sum += *cl.map_shared_rank(part + row * npc + j, qq);
+            p.v[(long long)tok[row] * p.ld_v + j0 + j] = sum;
+        }
+        cl.sync();                                // no CTA reuses or leaves part while a peer reads it
     }
 }
 
@@ -699,10 +923,13 @@ struct ExpandParams {
     int ncg;       // column groups per item
     int bpu;       // column blocks per unit (1 .. kMaxBlocksPerUnit)
     const int *tile_ad;   // non-null: the plan's item masks name rows whose term the GEMM already added
+    const Unit *units;    // unit kernel: the plan's expand units (count plan[3])
 };
 
-__global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+// Rows of item `it` outside `fused` x column blocks b_first .. b_first + nb_req - 1.
+// report: this CTA flags an invalid adapter.
+__device__ __forceinline__ void expand_unit(const ExpandParams &p, const Item &it, unsigned fused, int b_first,
+                                            int nb_req, bool report, uint8_t *smem_raw) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int yp = kNb + 8;                  // bf16 per smem row of y and B tiles
     const int kpc = p.kpc, vp = p.kpc + 8;
@@ -713,17 +940,11 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     int *tok = reinterpret_cast<int *>(svl + kM * vp);                    // [kM]
     int *wtot = tok + kM;                                                 // [8]
     int *rec = wtot + 8;
-    int *scan = rec + p.pv.rec_ints;
 
-    if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
-    const int cg = blockIdx.x % p.ncg;
-    const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
-    if (it.a < 0 || it.nt <= 0) return;
-    const unsigned fused = (p.tile_ad && p.src.plan) ? (unsigned)it.pad : 0u;
     const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
     if ((fused & all) == all) return;            // the GEMM added every row's term
     if (it.a >= p.pv.max_adapters) {
-        if (tid == 0 && cg == 0) flag(p.pv.status, LORA_DEV_BAD_ADAPTER);
+        if (tid == 0 && report) flag(p.pv.status, LORA_DEV_BAD_ADAPTER);
         return;
     }
     // the record and the item's tokens load together
@@ -742,7 +963,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     }
     __syncthreads();
     if (rec[0] < 0) {
-        if (tid == 0 && cg == 0) flag(p.pv.status, LORA_DEV_BAD_ADAPTER);
+        if (tid == 0 && report) flag(p.pv.status, LORA_DEV_BAD_ADAPTER);
         return;
     }
     const int nt = wtot[0];
@@ -751,8 +972,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     const int r = min(r_rec, p.ld_v);
     const float scale = __int_as_float(rec[1]);
     const int nb_total = (p.h_out + kNb - 1) / kNb;
-    const int b_first = cg * p.bpu;
-    const int nb = min(p.bpu, nb_total - b_first);
+    const int nb = min(nb_req, nb_total - b_first);
     if (nb <= 0 || r <= 0) return;
     const int mg = warp & 1, nh = warp >> 1;
     const int g = lane >> 2, q = lane & 3;
@@ -899,6 +1119,37 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     }
 }
 
+__global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int kpc = p.kpc, vp = p.kpc + 8;
+    constexpr int yp = kNb + 8;
+    int *wtot = reinterpret_cast<int *>(reinterpret_cast<__nv_bfloat16 *>(smem_raw) + kStagesE * kM * yp +
+                                        kStagesE * kpc * yp + 2 * kM * vp) + kM;
+    int *scan = wtot + 8 + p.pv.rec_ints;
+    if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    const int cg = blockIdx.x % p.ncg;
+    const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
+    if (it.a < 0 || it.nt <= 0) return;
+    const unsigned fused = (p.tile_ad && p.src.plan) ? (unsigned)it.pad : 0u;
+    expand_unit(p, it, fused, cg * p.bpu, p.bpu, cg == 0, smem_raw);
+}
+
+// Layer plans: persistent CTAs walk the plan's expand units (costly ones first,
+// snake order: CTA c takes units c, 2G - 1 - c, 2G + c, ...).
+__global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_units_kernel(ExpandParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int n_units = p.src.plan[3];
+    const int G = gridDim.x, c = blockIdx.x;
+    for (int k = 0;; ++k) {
+        const int u = k * G + ((k & 1) ? G - 1 - c : c);
+        if (u >= n_units) break;
+        const Unit un = p.units[u];
+        __syncthreads();                          // the previous unit's readers of shared memory are done
+        const Item it{un.a, un.off, un.info & 63, un.pad};
+        expand_unit(p, it, (unsigned)un.pad, un.info >> 10, (un.info >> 6) & 15, false, smem_raw);
+    }
+}
+
 // Upper bound on items: every non-empty segment (or adapter) has at least
 // one chunk, and the chunks together cover T tokens.
 int item_bound(int groups, int T) { return std::min(groups, T) + (T + kM - 1) / kM; }
@@ -913,33 +1164,61 @@ bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S) {
     return pool->dtype == LORA_BF16 && h_out % 8 == 0 && S <= kMaxS;
 }
 
-size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T) {
+// Plan layout in ints from its start: header [n_items, n_work, n_shrink_units,
+// n_expand_units], perm[T], items, M-tile adapters, work items, then (layer
+// plans) shrink and expand units.  Every array starts 16-byte aligned.
+struct PlanLayout {
+    int max_items, max_su, max_eu;
+    size_t tiles, work, su, eu, total;   // offsets in ints; total bytes
+};
+
+// Ranks per shrink CTA of the 128-thread kernels.
+static int shrink_npc(const lora_pool *pool) { return std::min(32, (pool->max_rank + 15) / 16 * 16); }
+
+static PlanLayout plan_layout(const lora_pool *pool, int matrix, int T) {
+    PlanLayout L;
     const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
     const int n_tiles = (T + kTileRows - 1) / kTileRows;
-    return (size_t)(4 + ((T + 3) & ~3)) * 4 + (size_t)2 * item_bound(n_ids, T) * sizeof(Item) +
-           (size_t)((n_tiles + 3) & ~3) * 4 + 64;
+    const int item_ints = (int)(sizeof(Item) / sizeof(int));
+    L.max_items = item_bound(n_ids, T);
+    L.max_su = L.max_items * 2 * ((pool->max_rank + shrink_npc(pool) - 1) / shrink_npc(pool));
+    L.max_eu = L.max_items * ((std::max(0, pool->mat_h_out[matrix]) + kNb - 1) / kNb);
+    L.tiles = 4 + (size_t)((T + 3) & ~3) + (size_t)L.max_items * item_ints;
+    L.work = L.tiles + (size_t)((n_tiles + 3) & ~3);
+    L.su = L.work + (size_t)L.max_items * item_ints;
+    L.eu = L.su + (size_t)L.max_su * item_ints;
+    L.total = (L.eu + (size_t)L.max_eu * item_ints) * 4 + 64;
+    return L;
 }
 
-// The plan's compacted work items (after its M-tile array, 16-byte aligned).
-static Item *sgmv_plan_work(const lora_pool *pool, int matrix, int T, int *plan) {
-    const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
-    const int n_tiles = (T + kTileRows - 1) / kTileRows;
-    return reinterpret_cast<Item *>(plan + 4 + ((T + 3) & ~3) + item_bound(n_ids, T) * (int)(sizeof(Item) / sizeof(int)) +
-                                    ((n_tiles + 3) & ~3));
-}
+size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T) { return plan_layout(pool, matrix, T).total; }
 
 int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan) {
-    const int n_ids = std::max(1, pool->mat_n_ids[matrix]);
-    return plan + 4 + ((T + 3) & ~3) + item_bound(n_ids, T) * (int)(sizeof(Item) / sizeof(int));
+    return plan + plan_layout(pool, matrix, T).tiles;
 }
 
-bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S) {
+static Item *sgmv_plan_work(const lora_pool *pool, int matrix, int T, int *plan) {
+    return reinterpret_cast<Item *>(plan + plan_layout(pool, matrix, T).work);
+}
+
+// Shared memory of the plan kernel: the counting-sort area, the scan words and,
+// for layer plans, the unit-building arrays.
+static size_t plan_smem(const lora_pool *pool, int matrix, int S, int T, bool units, int *body) {
     const int n_ids = pool->mat_n_ids[matrix];
-    return n_ids > 0 && S <= kMaxS && (size_t)(3 * n_ids + 3 * S) * 4 + 256 <= 160 * 1024;
+    *body = (3 * n_ids + 3 * S + 1 + 3) & ~3;
+    size_t ints = (size_t)*body + ((kPlanThreads / 32 + 2 + 3) & ~3);
+    if (units) ints += (size_t)9 * plan_layout(pool, matrix, T).max_items + 4 * (kPlanThreads / 32 + 1);
+    return ints * 4;
+}
+
+bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S, int T, bool units) {
+    int body;
+    return pool->mat_n_ids[matrix] > 0 && S <= kMaxS && plan_smem(pool, matrix, S, T, units, &body) <= 160 * 1024;
 }
 
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
                      int *plan, cudaStream_t st, int *tile_ad) {
+    const PlanLayout L = plan_layout(pool, matrix, T);
     PlanParams p;
     p.seg_starts = seg_starts;
     p.seg_adapter = seg_adapter;
@@ -948,13 +1227,19 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.n_ids = pool->mat_n_ids[matrix];
     p.status = pool->d_status;
     p.plan = plan;
-    p.max_items = item_bound(p.n_ids, T);
+    p.max_items = L.max_items;
     p.pv = pool->view();
     p.m = matrix;
     p.tile_ad = tile_ad;
     p.n_tiles = (T + kTileRows - 1) / kTileRows;
-    p.work = tile_ad ? sgmv_plan_work(pool, matrix, T, plan) : nullptr;
-    const size_t smem = (size_t)(3 * p.n_ids + 3 * S + 1 + kPlanThreads / 32 + 2) * 4;
+    p.work = tile_ad ? reinterpret_cast<Item *>(plan + L.work) : nullptr;
+    p.su = tile_ad ? reinterpret_cast<Unit *>(plan + L.su) : nullptr;
+    p.eu = tile_ad ? reinterpret_cast<Unit *>(plan + L.eu) : nullptr;
+    p.npc_s = shrink_npc(pool);
+    p.nb_total = (std::max(0, pool->mat_h_out[matrix]) + kNb - 1) / kNb;
+    p.bpu = 4;
+    p.rank_cap = pool->max_rank;
+    const size_t smem = plan_smem(pool, matrix, S, T, tile_ad != nullptr, &p.body);
     static size_t configured = 0;
     if (smem > configured) {
         if (cudaFuncSetAttribute(sgmv_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -982,6 +1267,43 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
     p.v = v;
     p.ld_v = ld_v;
     const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
+    if (skip_fused && plan) {
+        // layer plan: persistent clusters over the plan's shrink units, K split over the cluster
+        p.npc = shrink_npc(pool);
+        p.alias_bytes = 0;
+        p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).su);
+        const size_t smem = (size_t)kStagesS * (kRowsS + p.npc) * (kKs + 8) * 2 + (size_t)4 * 16 * p.npc * 4 +
+                            (size_t)(kRowsS + p.pv.rec_ints) * 4 + 16;
+        static size_t configured_u = 0;
+        static int occ = 0;
+        if (smem > configured_u) {
+            if (cudaFuncSetAttribute(sgmv_shrink_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgmv_shrink_units_kernel, kThreadsS, smem) !=
+                    cudaSuccess)
+                return LORA_ERR_CUDA;
+            configured_u = smem;
+        }
+        const int nk = h_in / kKs;
+        const int ks = nk >= 16 ? 2 : 1;       // measured: 2 beats 1 and 4 (4 leaves too few clusters)
+        const int clusters = std::max(1, num_sms() * std::max(1, occ) / ks);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ks, clusters, 1);
+        cfg.blockDim = dim3(kThreadsS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = ks;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_shrink_units_kernel, p);
+        count_launch();
+        return cuda_status(e != cudaSuccess ? e : cudaGetLastError());
+    }
+    p.units = nullptr;
     if (pool->max_rank > 32 && !plan) {
         // ranks above 32 in a segment table: whole items and 64-rank chunks per CTA
         p.npc = std::min(64, (pool->max_rank + 15) / 16 * 16);
@@ -1049,6 +1371,24 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
             return LORA_ERR_CUDA;
         configured = smem;
     }
+    if (tile_ad && plan) {
+        // layer plan: persistent CTAs over the plan's expand units
+        p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).eu);
+        static size_t configured_u = 0;
+        static int occ = 0;
+        if (smem > configured_u) {
+            if (cudaFuncSetAttribute(sgmv_expand_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgmv_expand_units_kernel, kThreadsE, smem) !=
+                    cudaSuccess)
+                return LORA_ERR_CUDA;
+            configured_u = smem;
+        }
+        sgmv_expand_units_kernel<<<num_sms() * std::max(1, occ), kThreadsE, smem, st>>>(p);
+        count_launch();
+        return cuda_status(cudaGetLastError());
+    }
+    p.units = nullptr;
     const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
     sgmv_expand_kernel<<<item_bound(groups, T) * p.ncg, kThreadsE, smem, st>>>(p);
     count_launch();
