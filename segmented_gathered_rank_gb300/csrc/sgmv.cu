@@ -293,6 +293,8 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     int *segoff = ibase + p.n_ids;       // [S] offset of each segment within its adapter's tokens
     int *sb = segoff + p.S;              // [S + 1] segment bounds, clamped into [0, T]
     int *sa = sb + p.S + 1;              // [S] segment adapters (-1: none or invalid)
+    int *arank = sa + p.S;               // with tile_ad: [n_ids] each adapter's rank on the matrix
+    int *sperm = arank + p.n_ids;        // with tile_ad: [T] copy of the token permutation
     int *wtot = sm + p.body;             // [kPlanThreads / 32 + 1], then the work count
     // with units: [max_items] int4 work items, int4 unit counts and ranks, after the counters
     int4 *sitem = reinterpret_cast<int4 *>(sm + p.body + ((kPlanThreads / 32 + 2 + 3) & ~3));
@@ -301,15 +303,26 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     int *srank = reinterpret_cast<int *>(wtot4 + kPlanThreads / 32 + 1);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = kPlanThreads / 32;
-    check_segments(p.seg_starts, p.S, p.T, p.status);
-    for (int i = tid; i < p.n_ids; i += kPlanThreads) cnt[i] = 0;
-    for (int s = tid; s <= p.S; s += kPlanThreads) sb[s] = min(max(p.seg_starts[s], 0), p.T);
+    // one round of global loads: segment bounds (checked as they arrive), segment
+    // adapters and, with tile_ad, every adapter's rank
+    bool bad = false;
+    for (int i = tid; i < p.n_ids; i += kPlanThreads) {
+        cnt[i] = 0;
+        if (p.tile_ad) arank[i] = p.pv.table[((long long)i * p.pv.n_matrices + p.m) * p.pv.rec_ints];
+    }
+    for (int s = tid; s <= p.S; s += kPlanThreads) {
+        const int b0 = p.seg_starts[s];
+        if (s < p.S) bad |= p.seg_starts[s + 1] < b0;
+        if (s == 0) bad |= b0 != 0;
+        if (s == p.S) bad |= b0 != p.T;
+        sb[s] = min(max(b0, 0), p.T);
+    }
     for (int s = tid; s < p.S; s += kPlanThreads) {
         const int a = p.seg_adapter[s];
         sa[s] = a < p.n_ids ? a : -1;
         if (a >= p.n_ids) flag(p.status, LORA_DEV_BAD_ADAPTER);      // never loaded on this matrix
     }
-    __syncthreads();
+    if (__syncthreads_or(bad) && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENTS);
     // one atomic per segment: its tokens stay contiguous and in order
     for (int s = tid; s < p.S; s += kPlanThreads) {
         const int n = sb[s + 1] - sb[s];
@@ -326,6 +339,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     int *perm = p.plan + 4;
     Item *items = reinterpret_cast<Item *>(p.plan + 4 + ((p.T + 3) & ~3));
     // one thread per item: its adapter is the last whose first item index is <= it
+    Item first_item{-1, 0, 0, 0};        // this thread's item of the first round (reused below)
     for (int i = tid; i < min(n_items, p.max_items); i += kPlanThreads) {
         int lo = 0, hi = p.n_ids - 1;
         while (lo < hi) {
@@ -337,6 +351,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         const int off = base[a] + c * kM;
         const int nt = max(0, min(min(kM, n - c * kM), p.T - off));
         items[i] = Item{nt > 0 ? a : -1, off, nt, 0};
+        if (i == tid) first_item = items[i];
     }
     if (tid == 0) p.plan[0] = min(n_items, p.max_items);
     for (int i = n_items + tid; i < p.max_items; i += kPlanThreads) items[i] = Item{-1, 0, 0, 0};
@@ -346,14 +361,20 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         if (segoff[s] < 0 || n > 32) continue;
         const int dst = base[sa[s]] + segoff[s];
         for (int i = 0; i < n; ++i)
-            if (dst + i < p.T) perm[dst + i] = sb[s] + i;
+            if (dst + i < p.T) {
+                perm[dst + i] = sb[s] + i;
+                if (p.tile_ad) sperm[dst + i] = sb[s] + i;
+            }
     }
     for (int s = warp; s < p.S; s += nwarps) {
         const int n = sb[s + 1] - sb[s];
         if (segoff[s] < 0 || n <= 32) continue;
         const int dst = base[sa[s]] + segoff[s];
         for (int i = lane; i < n; i += 32)
-            if (dst + i < p.T) perm[dst + i] = sb[s] + i;
+            if (dst + i < p.T) {
+                perm[dst + i] = sb[s] + i;
+                if (p.tile_ad) sperm[dst + i] = sb[s] + i;
+            }
     }
     if (!p.tile_ad) return;
     int *wcount = wtot + nwarps + 1;        // past block_scan's words
@@ -380,8 +401,8 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
             else if (sa[s] != a) uniform = false;
         }
         int out = -1;
-        if (uniform && a >= 0 && a < p.pv.max_adapters) {
-            const int rank = p.pv.table[((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints];
+        if (uniform && a >= 0 && a < p.n_ids) {
+            const int rank = arank[a];
             if (rank >= 1 && rank <= kFuseMaxRank) out = a;
         }
         p.tile_ad[mb] = out;
@@ -398,16 +419,16 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         Item w{-1, 0, 0, 0};
         int rank = 0;
         if (i < nitems) {
-            const Item it = items[i];
+            const Item it = i0 == 0 ? first_item : items[i];
             if (it.a >= 0) {
-                if (p.su) rank = p.pv.table[((long long)it.a * p.pv.n_matrices + p.m) * p.pv.rec_ints];
+                rank = arank[it.a];
                 int tk[kM];
 #pragma unroll
-                for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? perm[it.off + k] : -1;
+                for (int k = 0; k < kM; ++k) tk[k] = k < it.nt ? sperm[it.off + k] : -1;
                 unsigned mask = 0;
 #pragma unroll
                 for (int k = 0; k < kM; ++k)
-                    if (tk[k] >= 0 && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0)
+                    if (tk[k] >= 0 && tk[k] < p.T && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0)
                         mask |= 1u << k;
                 items[i].pad = (int)mask;
                 const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
@@ -1205,7 +1226,7 @@ static Item *sgmv_plan_work(const lora_pool *pool, int matrix, int T, int *plan)
 // for layer plans, the unit-building arrays.
 static size_t plan_smem(const lora_pool *pool, int matrix, int S, int T, bool units, int *body) {
     const int n_ids = pool->mat_n_ids[matrix];
-    *body = (3 * n_ids + 3 * S + 1 + 3) & ~3;
+    *body = (3 * n_ids + 3 * S + 1 + (units ? n_ids + T : 0) + 3) & ~3;
     size_t ints = (size_t)*body + ((kPlanThreads / 32 + 2 + 3) & ~3);
     if (units) ints += (size_t)9 * plan_layout(pool, matrix, T).max_items + 4 * (kPlanThreads / 32 + 1);
     return ints * 4;
