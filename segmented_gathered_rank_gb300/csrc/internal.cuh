@@ -32,7 +32,7 @@ constexpr int kRecHeader = 4;
 
 // The tensor-core GEMM adds the adapter term itself for an M-tile of
 // kFuseTileRows rows that all use one adapter of rank <= kFuseMaxRank (in
-// 64-rank rounds); the plan marks such tiles, the tensor-core shrink computes
+// 32-rank rounds); the plan marks such tiles, the tensor-core shrink computes
 // their v, and the warp-MMA shrink and the expand skip their rows.
 constexpr int kFuseTileRows = 128;
 constexpr int kFuseMaxRank = 128;

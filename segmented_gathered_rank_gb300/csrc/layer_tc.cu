@@ -10,13 +10,14 @@
 //
 // Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles,
 // K in steps of 64.  Warp 0 (one lane) streams x and W tiles into a 4-stage
-// (fused: 3-stage) shared-memory ring with TMA (128-byte swizzle); warp 1
+// shared-memory ring with TMA (128-byte swizzle); warp 1
 // (one lane) issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of
 // two TMEM accumulators (2 x 256 columns) and commits each ring slot back to
 // the producer and each finished accumulator to the epilogue; warps 2-5 read
 // the accumulator with tcgen05.ld (each warp its 32-lane TMEM sub-partition,
 // one row per thread), round to bf16 and store, and in the fused variant
-// stage the next uniform tile's s * v and B operands.  The two accumulators
+// stage the next uniform tile's s * v and B operands (32 ranks per round,
+// 64-byte swizzle, 32 KB beside the ring).  The two accumulators
 // let the epilogue of one tile overlap the main loop of the next.
 //
 // Every mbarrier wait is bounded (by the global timer); a wait that gives up
@@ -42,8 +43,13 @@ constexpr int kThreadsTC = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
-constexpr int A2_BYTES = BM * 64 * 2;   // s * v tile, one 64-wide K chunk (high or residual part)
-constexpr int B2_BYTES = BN * 64 * 2;   // B rows of the tile's columns, transposed to K-major
+// The fused tile's low-rank term enters the accumulator in rounds of kRound ranks,
+// staged K-major with 64-byte swizzling; 32-rank rounds keep the operands at
+// 32 KB, which leaves room for a 4-stage ring (4 x 48 KB) in 227 KB.
+constexpr int kRound = 32;
+constexpr int kMaxRounds = (kFuseMaxRank + kRound - 1) / kRound;
+constexpr int A2_BYTES = BM * kRound * 2;   // s * v tile, one round (high or residual part)
+constexpr int B2_BYTES = BN * kRound * 2;   // B rows of the tile's columns, transposed to K-major
 
 struct LayerTcParams {
     int T, N, K;
@@ -65,7 +71,7 @@ struct Ctrl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
-    uint64_t aready;      // one 64-rank round of a tile's adapter operands is in shared memory
+    uint64_t aready;      // one round of a tile's adapter operands is in shared memory
     uint64_t aconsumed;   // the MMAs of that round have read it
     uint32_t tmem_base;
     int abort;
@@ -80,23 +86,24 @@ __device__ __forceinline__ uint32_t swz128(int row, int c) {
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + (((c ^ row) & 7) << 4));
 }
 
-// Epilogue warps (128 threads): stage round `round` (ranks 64*round ..
-// 64*round+63) of the adapter term's operands of `tile`; returns the tile's
+// Epilogue warps (128 threads): stage round `round` (ranks kRound*round ..
+// +kRound-1) of the adapter term's operands of `tile`; returns the tile's
 // number of rounds.  A2hi/A2lo: s * v of the tile's rows (bf16 high part /
 // residual), K-major; B2: row n holds B_a[j][n0 + n] (the B rows transposed),
 // K-major.  Every global load of a round is independent of the others but
 // for the page ids, so a round costs about two memory round trips.
 // What round 0 of a tile looks up for every round of it (one thread's share):
-// the adapter's rank and scale and the B page ids of ranks lane + 32 h + 64 rd.
+// the adapter's rank and scale and the B page ids of ranks lane + kRound * rd.
 struct FillCache {
     int r;
     float s;
-    int page[2][2];
+    int page[kMaxRounds];
 };
 
 template <int ST>
 __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t *a2hi, uint8_t *a2lo, uint8_t *b2,
                             Ctrl<ST> *ctrl, int ethr, FillCache &fc) {
+    static_assert(kRound == 32, "one rank of a round per lane");
     const int mb = tile % p.num_m, nb = tile / p.num_m;
     const int lane = ethr & 31, w = ethr >> 5;
     if (round == 0) {
@@ -111,18 +118,16 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
             if (r > 0) fc.s = __int_as_float(rec[1]);
             // every round's page ids now: a later round then costs one memory round trip
 #pragma unroll
-            for (int rd = 0; rd < 2; ++rd)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int j = lane + 32 * h + 64 * rd;
-                    const int pg = j < r ? rec[kRecHeader + r + j] : 0;
-                    fc.page[rd][h] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
-                }
+            for (int rd = 0; rd < kMaxRounds; ++rd) {
+                const int j = lane + kRound * rd;
+                const int pg = j < r ? rec[kRecHeader + r + j] : 0;
+                fc.page[rd] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
+            }
         }
     }
     const int r = fc.r;
-    const int rounds = (r + 63) / 64;
-    const int j0 = round * 64, rn = max(0, min(64, r - j0));
+    const int rounds = (r + kRound - 1) / kRound;
+    const int j0 = round * kRound, rn = max(0, min(kRound, r - j0));
     const int kpad = (rn + 15) & ~15;
     if (ethr == 0) {
         ctrl->akpad = kpad;
@@ -130,8 +135,10 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
     }
     if (kpad == 0) return rounds;
     const float s = fc.s;
-    // B page ids of this lane's ranks (lane, lane + 32) in this round
-    const int page[2] = {fc.page[round & 1][0], fc.page[round & 1][1]};
+    int page = 0;     // B page id of this lane's rank (lane) in this round
+#pragma unroll
+    for (int rd = 0; rd < kMaxRounds; ++rd)
+        if (rd == round) page = fc.page[rd];
     // A2: row ethr of the tile, s * v split into bf16 high part and residual
     {
         const int row = mb * BM + ethr;
@@ -139,7 +146,7 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
         const float *vrow = p.v + (long long)(live ? row : 0) * p.ld_v + j0;
         const bool vec = (p.ld_v & 3) == 0;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kRound / 8; ++c) {
             if (c * 8 >= kpad) break;
             float vv[8];
             const float *vp = vrow + c * 8;
@@ -167,17 +174,15 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
                 hi[e] = __float2bfloat16_rn(val);
                 lo[e] = __float2bfloat16_rn(val - __bfloat162float(hi[e]));
             }
-            *reinterpret_cast<uint4 *>(a2hi + swz128(ethr, c)) = hi4;
-            *reinterpret_cast<uint4 *>(a2lo + swz128(ethr, c)) = lo4;
+            *reinterpret_cast<uint4 *>(a2hi + swz64(ethr, c)) = hi4;
+            *reinterpret_cast<uint4 *>(a2lo + swz64(ethr, c)) = lo4;
         }
     }
-    // B2: warp w loads 8-column groups g = w, w + 4, ... of the ranks lane and
-    // lane + 32 (16-byte loads of page rows), then writes them transposed.
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int j = lane + 32 * h;
-        if (j >= kpad) break;
-        const __nv_bfloat16 *prow = page_row<__nv_bfloat16>(p.pv, page[h]);
+    // B2: warp w loads 8-column groups g = w, w + 4, ... of rank `lane` (16-byte
+    // loads of a page row), then writes them transposed.
+    if (lane < kpad) {
+        const int j = lane;
+        const __nv_bfloat16 *prow = page_row<__nv_bfloat16>(p.pv, page);
         uint4 d[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -190,7 +195,7 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
             const __nv_bfloat16 *e8 = reinterpret_cast<const __nv_bfloat16 *>(&d[q]);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<__nv_bfloat16 *>(b2 + swz128(n0 + e, j >> 3) + (j & 7) * 2) = e8[e];
+                *reinterpret_cast<__nv_bfloat16 *>(b2 + swz64(n0 + e, j >> 3) + (j & 7) * 2) = e8[e];
         }
     }
     return rounds;
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                 }
                 if (ok && FUSE) {
-                    // the tile's low-rank term, 64 ranks per round:
+                    // the tile's low-rank term, kRound ranks per round:
                     // acc += (s v)_hi . B + (s v)_lo . B over the round's ranks
                     const uint32_t ah = smem_u32(a2hi), al = smem_u32(a2lo), bb = smem_u32(b2);
                     int rounds = 1;
@@ -327,8 +332,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         if (rd == 0) rounds = ctrl->arounds;
                         const int kpad = ctrl->akpad;
                         for (int kk = 0; kk < kpad / 16; ++kk) {
-                            mma_bf16(d, desc_kmajor_sw128(ah + kk * 32), desc_kmajor_sw128(bb + kk * 32), IDESC, 1);
-                            mma_bf16(d, desc_kmajor_sw128(al + kk * 32), desc_kmajor_sw128(bb + kk * 32), IDESC, 1);
+                            mma_bf16(d, desc_kmajor_sw64(ah + kk * 32), desc_kmajor_sw64(bb + kk * 32), IDESC, 1);
+                            mma_bf16(d, desc_kmajor_sw64(al + kk * 32), desc_kmajor_sw64(bb + kk * 32), IDESC, 1);
                         }
                     }
                     if (!ok) break;
@@ -863,7 +868,7 @@ int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, co
     p.m = matrix;
     p.v = v;
     p.ld_v = ld_v;
-    if (tile_ad) return launch_gemm_variant<3, true>(tmx, tmw, p, st);
+    if (tile_ad) return launch_gemm_variant<4, true>(tmx, tmw, p, st);
     return launch_gemm_variant<4, false>(tmx, tmw, p, st);
 }
 

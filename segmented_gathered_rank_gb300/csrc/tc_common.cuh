@@ -184,6 +184,24 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Shared-memory operand descriptor: K-major tile with 64-byte swizzling (rows of
+// 32 bf16, 8-row / 512-byte swizzle atoms), as written by swz64 below.
+__device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+    d |= (uint64_t)(16u >> 4) << 16;                // leading-dimension offset (unused with this swizzle)
+    d |= (uint64_t)(512u >> 4) << 32;               // stride between 8-row atoms
+    d |= (uint64_t)1 << 46;                         // descriptor version for sm_100-family
+    d |= (uint64_t)4 << 61;                         // 64-byte swizzle
+    return d;
+}
+
+// Byte offset of 16-byte chunk c (0..3) of row `row` in a K-major tile with
+// 64-byte swizzling: chunk index XOR bits 1-2 of the row.
+__device__ __forceinline__ uint32_t swz64(int row, int c) {
+    return (uint32_t)((row >> 3) * 512 + (row & 7) * 64 + (((c ^ (row >> 1)) & 3) << 4));
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4)                      // D: fp32
