@@ -174,6 +174,14 @@ size_t lora_layer_forward_workspace_size(const lora_pool *pool, int matrix, int 
  * adapter (or with an invalid one) get the base term only.
  * workspace: device scratch of at least lora_layer_forward_workspace_size()
  * bytes, owned by the caller, contents undefined on entry and exit.
+ * Streams: part of the call's work (the shrink of rows whose M-tile is not
+ * fused into the GEMM) may run on an internal stream, one per host thread
+ * and device, that the call forks from `stream` and joins back to it with
+ * events; the call's work as a whole stays ordered after earlier work on
+ * `stream` and before later work on it, and under stream capture the fork
+ * and join become graph edges.  The internal stream and its events are
+ * created by the first such call on a thread: make that call outside stream
+ * capture.
  * Errors: LORA_ERR_ARG (includes ws_bytes too small), LORA_ERR_SHAPE.
  */
 int lora_layer_forward(lora_pool *pool, int matrix, const void *x, const void *W, void *y,
