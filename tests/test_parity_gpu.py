@@ -399,3 +399,38 @@ def test_repeated_calls_are_bit_identical():
     vs = [run_sgmv(w)[0] for _ in range(2)]
     mask = written_mask(w, w.max_rank)
     assert np.array_equal(vs[0][mask], vs[1][mask])
+
+
+def test_layer_in_cuda_graph_on_side_stream_matches_eager():
+    # The layer call forks part of its work onto an internal stream and joins it back:
+    # captured into a CUDA graph on a non-default stream and replayed, it must give
+    # exactly what the eager call gives (and the oracle's answer), and it must leave
+    # nothing unjoined (capture would fail).
+    w = I.random_case(43, T=700, lengths=[256, 128, 1, 1, 1, 313], h_in=1024, h_out=512, ranks=[128, 16, 96])
+    with H.DevicePool(w, matrices=[0]) as dp:
+        ss, sa = _tables(w)
+        x = H.to_device(w.x(0), w.dtype)
+        Wh = w.W(0)
+        Wd = H.to_device(Wh, w.dtype)
+        ws = torch.empty(L.lora_layer_forward_workspace_size(dp.handle, 0, w.S, w.T), dtype=torch.uint8,
+                         device="cuda")
+        y_eager = torch.full((w.T, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        L.lora_layer_forward(dp.handle, 0, x, Wd, y_eager, ss, sa, w.S, w.T, ws)
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        y_graph = torch.full((w.T, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                L.lora_layer_forward(dp.handle, 0, x, Wd, y_graph, ss, sa, w.S, w.T, ws,
+                                     stream=torch.cuda.current_stream())
+        for _ in range(2):
+            y_graph.fill_(float("nan"))
+            g.replay()
+        torch.cuda.synchronize()
+        word = dp.check_device_status()
+    ye, yg = H.to_host(y_eager), H.to_host(y_graph)
+    assert word == 0
+    assert not np.isnan(yg).any() and np.array_equal(ye, yg)
+    yr, st = oracle_delta(w, 0, None, W=Wh)
+    assert st == 0 and rel_err(yg, yr) <= TOL_Y[w.dtype]
