@@ -86,12 +86,13 @@ __device__ __forceinline__ uint32_t swz128(int row, int c) {
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + (((c ^ row) & 7) << 4));
 }
 
-// Epilogue warps (128 threads): stage round `round` (ranks kRound*round ..
-// +kRound-1) of the adapter term's operands of `tile`; returns the tile's
-// number of rounds.  A2hi/A2lo: s * v of the tile's rows (bf16 high part /
-// residual), K-major; B2: row n holds B_a[j][n0 + n] (the B rows transposed),
-// K-major.  Every global load of a round is independent of the others but
-// for the page ids, so a round costs about two memory round trips.
+// Epilogue warps (128 threads) stage round `round` (ranks kRound*round ..
+// +kRound-1) of the adapter term's operands of a tile in two steps: its global
+// loads into registers (load_round), then the bf16 conversion and the
+// swizzled shared-memory stores (store_round).  A2hi/A2lo: s * v of the tile's
+// rows (bf16 high part / residual), K-major; B2: row n holds B_a[j][n0 + n]
+// (the B rows transposed), K-major.  The next round's loads are issued as
+// soon as a round is handed to the MMA warp, so they overlap its MMAs.
 // What round 0 of a tile looks up for every round of it (one thread's share):
 // the adapter's rank and scale and the B page ids of ranks lane + kRound * rd.
 struct FillCache {
@@ -100,34 +101,80 @@ struct FillCache {
     int page[kMaxRounds];
 };
 
-template <int ST>
-__device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t *a2hi, uint8_t *a2lo, uint8_t *b2,
-                            Ctrl<ST> *ctrl, int ethr, FillCache &fc) {
+// One thread's share of a round: its row's v values and its rank's B columns.
+struct RoundRegs {
+    float4 v[kRound / 4];
+    uint4 b[8];
+};
+
+// Rank, scale and page ids of the tile's adapter (round 0 only).
+__device__ __forceinline__ void lookup_adapter(const LayerTcParams &p, int tile, int lane, FillCache &fc) {
+    const int mb = tile % p.num_m;
+    const int a = p.tile_ad[mb];
+    fc.r = 0;
+    fc.s = 0.f;
+    if (a >= 0 && a < p.pv.max_adapters) {
+        const int *rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
+        int r = rec[0];
+        if (r < 1 || r > kFuseMaxRank || r > p.ld_v) r = 0;
+        fc.r = r;
+        if (r > 0) fc.s = __int_as_float(rec[1]);
+#pragma unroll
+        for (int rd = 0; rd < kMaxRounds; ++rd) {
+            const int j = lane + kRound * rd;
+            const int pg = j < r ? rec[kRecHeader + r + j] : 0;
+            fc.page[rd] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
+        }
+    }
+}
+
+__device__ __forceinline__ void load_round(const LayerTcParams &p, int tile, int round, const FillCache &fc,
+                                           int ethr, RoundRegs &g) {
     static_assert(kRound == 32, "one rank of a round per lane");
     const int mb = tile % p.num_m, nb = tile / p.num_m;
     const int lane = ethr & 31, w = ethr >> 5;
-    if (round == 0) {
-        const int a = p.tile_ad[mb];
-        fc.r = 0;
-        fc.s = 0.f;
-        if (a >= 0 && a < p.pv.max_adapters) {
-            const int *rec = p.pv.table + ((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints;
-            int r = rec[0];
-            if (r < 1 || r > kFuseMaxRank || r > p.ld_v) r = 0;
-            fc.r = r;
-            if (r > 0) fc.s = __int_as_float(rec[1]);
-            // every round's page ids now: a later round then costs one memory round trip
+    const int j0 = round * kRound, rn = max(0, min(kRound, fc.r - j0));
+    const int kpad = (rn + 15) & ~15;
+    // v: row ethr of the tile
+    const int row = mb * BM + ethr;
+    const bool live = row < p.T;
+    const float *vrow = p.v + (long long)(live ? row : 0) * p.ld_v + j0;
+    const bool vec = (p.ld_v & 3) == 0;
 #pragma unroll
-            for (int rd = 0; rd < kMaxRounds; ++rd) {
-                const int j = lane + kRound * rd;
-                const int pg = j < r ? rec[kRecHeader + r + j] : 0;
-                fc.page[rd] = pg < 0 ? 0 : (pg >= p.pv.n_pages ? p.pv.n_pages - 1 : pg);
+    for (int c = 0; c < kRound / 4; ++c) {
+        g.v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && c * 4 < rn) {
+            if (vec) {                       // ranks past rn hold zeros after the conversion (float4 over-read)
+                g.v[c] = *reinterpret_cast<const float4 *>(vrow + c * 4);
+            } else {
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int u = 0; u < 4; ++u)
+                    if (c * 4 + u < rn) e[u] = vrow[c * 4 + u];
+                g.v[c] = make_float4(e[0], e[1], e[2], e[3]);
             }
         }
     }
-    const int r = fc.r;
-    const int rounds = (r + kRound - 1) / kRound;
-    const int j0 = round * kRound, rn = max(0, min(kRound, r - j0));
+    // B: rank `lane` of the round, 8-column groups w, w + 4, ... of the tile's columns
+    int page = 0;
+#pragma unroll
+    for (int rd = 0; rd < kMaxRounds; ++rd)
+        if (rd == round) page = fc.page[rd];
+    const __nv_bfloat16 *prow = page_row<__nv_bfloat16>(p.pv, page);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int col = nb * BN + (w + 4 * q) * 8;
+        g.b[q] = (lane < rn && lane < kpad && col < p.N) ? *reinterpret_cast<const uint4 *>(prow + col)
+                                                         : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Writes the round's operands; returns the tile's number of rounds.
+template <int ST>
+__device__ int store_round(const FillCache &fc, int round, const RoundRegs &g, uint8_t *a2hi, uint8_t *a2lo,
+                           uint8_t *b2, Ctrl<ST> *ctrl, int ethr) {
+    const int lane = ethr & 31, w = ethr >> 5;
+    const int rounds = (fc.r + kRound - 1) / kRound;
+    const int j0 = round * kRound, rn = max(0, min(kRound, fc.r - j0));
     const int kpad = (rn + 15) & ~15;
     if (ethr == 0) {
         ctrl->akpad = kpad;
@@ -135,64 +182,30 @@ __device__ int fill_adapter(const LayerTcParams &p, int tile, int round, uint8_t
     }
     if (kpad == 0) return rounds;
     const float s = fc.s;
-    int page = 0;     // B page id of this lane's rank (lane) in this round
 #pragma unroll
-    for (int rd = 0; rd < kMaxRounds; ++rd)
-        if (rd == round) page = fc.page[rd];
-    // A2: row ethr of the tile, s * v split into bf16 high part and residual
-    {
-        const int row = mb * BM + ethr;
-        const bool live = row < p.T;
-        const float *vrow = p.v + (long long)(live ? row : 0) * p.ld_v + j0;
-        const bool vec = (p.ld_v & 3) == 0;
+    for (int c = 0; c < kRound / 8; ++c) {
+        if (c * 8 >= kpad) break;
+        const float vv[8] = {g.v[2 * c].x, g.v[2 * c].y, g.v[2 * c].z, g.v[2 * c].w,
+                             g.v[2 * c + 1].x, g.v[2 * c + 1].y, g.v[2 * c + 1].z, g.v[2 * c + 1].w};
+        uint4 hi4, lo4;
+        __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(&hi4);
+        __nv_bfloat16 *lo = reinterpret_cast<__nv_bfloat16 *>(&lo4);
 #pragma unroll
-        for (int c = 0; c < kRound / 8; ++c) {
-            if (c * 8 >= kpad) break;
-            float vv[8];
-            const float *vp = vrow + c * 8;
-            if (vec) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float4 f = (live && c * 8 + 4 * h < rn) ? *reinterpret_cast<const float4 *>(vp + 4 * h)
-                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                    vv[4 * h] = f.x;
-                    vv[4 * h + 1] = f.y;
-                    vv[4 * h + 2] = f.z;
-                    vv[4 * h + 3] = f.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vv[e] = (live && c * 8 + e < rn) ? vp[e] : 0.f;
-            }
-            uint4 hi4, lo4;
-            __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(&hi4);
-            __nv_bfloat16 *lo = reinterpret_cast<__nv_bfloat16 *>(&lo4);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = c * 8 + e;
-                const float val = j < rn ? s * vv[e] : 0.f;     // ranks past rn hold zeros (float4 over-read)
-                hi[e] = __float2bfloat16_rn(val);
-                lo[e] = __float2bfloat16_rn(val - __bfloat162float(hi[e]));
-            }
-            *reinterpret_cast<uint4 *>(a2hi + swz64(ethr, c)) = hi4;
-            *reinterpret_cast<uint4 *>(a2lo + swz64(ethr, c)) = lo4;
+        for (int e = 0; e < 8; ++e) {
+            const int j = c * 8 + e;
+            const float val = j < rn ? s * vv[e] : 0.f;
+            hi[e] = __float2bfloat16_rn(val);
+            lo[e] = __float2bfloat16_rn(val - __bfloat162float(hi[e]));
         }
+        *reinterpret_cast<uint4 *>(a2hi + swz64(ethr, c)) = hi4;
+        *reinterpret_cast<uint4 *>(a2lo + swz64(ethr, c)) = lo4;
     }
-    // B2: warp w loads 8-column groups g = w, w + 4, ... of rank `lane` (16-byte
-    // loads of a page row), then writes them transposed.
     if (lane < kpad) {
         const int j = lane;
-        const __nv_bfloat16 *prow = page_row<__nv_bfloat16>(p.pv, page);
-        uint4 d[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int col = nb * BN + (w + 4 * q) * 8;
-            d[q] = (j < rn && col < p.N) ? *reinterpret_cast<const uint4 *>(prow + col) : make_uint4(0, 0, 0, 0);
-        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int n0 = (w + 4 * q) * 8;
-            const __nv_bfloat16 *e8 = reinterpret_cast<const __nv_bfloat16 *>(&d[q]);
+            const __nv_bfloat16 *e8 = reinterpret_cast<const __nv_bfloat16 *>(&g.b[q]);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 *reinterpret_cast<__nv_bfloat16 *>(b2 + swz64(n0 + e, j >> 3) + (j & 7) * 2) = e8[e];
@@ -353,8 +366,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         bool staged_ok = true;
         // stage every round of a tile's adapter operands, handing each to the MMA warp
         auto stage_tile = [&](int t) {
-            int rounds = 1;
             FillCache fc;
+            RoundRegs g;
+            lookup_adapter(p, t, lane, fc);
+            const int rounds = max(1, (fc.r + kRound - 1) / kRound);
+            load_round(p, t, 0, fc, ethr, g);
             for (int rd = 0; rd < rounds; ++rd) {
                 if (rd > 0) {
                     const bool okc = wait_phase(&ctrl->aconsumed, n_consumed++ & 1u, abort);
@@ -364,11 +380,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         return;
                     }
                 }
-                rounds = fill_adapter<STAGES>(p, t, rd, a2hi, a2lo, b2, ctrl, ethr, fc);
-                if (rounds < 1) rounds = 1;
+                store_round<STAGES>(fc, rd, g, a2hi, a2lo, b2, ctrl, ethr);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctrl->aready);
+                if (rd + 1 < rounds) load_round(p, t, rd + 1, fc, ethr, g);   // overlaps round rd's MMAs
             }
         };
         if (FUSE && (int)blockIdx.x < p.num_tiles) stage_tile(blockIdx.x);
