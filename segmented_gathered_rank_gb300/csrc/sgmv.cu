@@ -1393,19 +1393,23 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
         configured = smem;
     }
     if (tile_ad && plan) {
-        // layer plan: persistent CTAs over the plan's expand units
+        // layer plan: persistent CTAs over the plan's expand units, in passes of at most 32
+        // ranks (a third CTA per SM; only units of ranks above 32 take more passes)
         p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).eu);
+        p.kpc = std::min(32, p.kpc);
+        const size_t smem_u = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
+                              (size_t)(kM + 8 + p.pv.rec_ints) * 4 + 16;
         static size_t configured_u = 0;
         static int occ = 0;
-        if (smem > configured_u) {
+        if (smem_u > configured_u) {
             if (cudaFuncSetAttribute(sgmv_expand_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgmv_expand_units_kernel, kThreadsE, smem) !=
+                                     (int)smem_u) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgmv_expand_units_kernel, kThreadsE, smem_u) !=
                     cudaSuccess)
                 return LORA_ERR_CUDA;
-            configured_u = smem;
+            configured_u = smem_u;
         }
-        sgmv_expand_units_kernel<<<num_sms() * std::max(1, occ), kThreadsE, smem, st>>>(p);
+        sgmv_expand_units_kernel<<<num_sms() * std::max(1, occ), kThreadsE, smem_u, st>>>(p);
         count_launch();
         return cuda_status(cudaGetLastError());
     }
