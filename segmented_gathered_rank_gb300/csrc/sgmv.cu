@@ -279,9 +279,9 @@ struct PlanParams {
 };
 
 // Column blocks per expand unit from an item's cost per block: its y rows,
-// read and written once per pass of up to 64 ranks, plus its B rows.
+// read and written once per pass of up to 32 ranks, plus its B rows.
 __device__ __forceinline__ int expand_bpu(int nt, int r, int bpu_cheap) {
-    const int cost = 2 * nt * ((r + 63) / 64) + r;
+    const int cost = 2 * nt * ((r + 31) / 32) + r;
     return cost >= 48 ? 1 : (cost >= 24 ? 2 : bpu_cheap);
 }
 
@@ -1258,7 +1258,7 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.eu = tile_ad ? reinterpret_cast<Unit *>(plan + L.eu) : nullptr;
     p.npc_s = shrink_npc(pool);
     p.nb_total = (std::max(0, pool->mat_h_out[matrix]) + kNb - 1) / kNb;
-    p.bpu = 4;
+    p.bpu = 8;
     p.rank_cap = pool->max_rank;
     const size_t smem = plan_smem(pool, matrix, S, T, tile_ad != nullptr, &p.body);
     static size_t configured = 0;
