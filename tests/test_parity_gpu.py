@@ -434,3 +434,26 @@ def test_layer_in_cuda_graph_on_side_stream_matches_eager():
     assert not np.isnan(yg).any() and np.array_equal(ye, yg)
     yr, st = oracle_delta(w, 0, None, W=Wh)
     assert st == 0 and rel_err(yg, yr) <= TOL_Y[w.dtype]
+
+
+def test_layer_more_items_than_plan_threads():
+    # 2600 one-token segments over 1500 adapters of mixed rank: over 1024 items and
+    # over 1024 work items, so every plan loop and scan runs more than one round
+    ranks = np.tile(np.array([4, 16, 32, 64, 8], np.int32), 300)
+    w = I.random_case(51, T=2600, decode=True, ranks=ranks, h_in=256, h_out=256)
+    y, Wh, word = run_layer(w)
+    assert word == 0
+    yr, st = oracle_delta(w, 0, None, W=Wh)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+
+
+def test_layer_one_segment_every_tile_fused():
+    # one 1000-token segment of one rank-64 adapter: every M-tile, the ragged last one too,
+    # is fused into the GEMM (two rounds each), the plan's tile flags are read from global
+    # memory (more tiles than its shared staging holds), and no row is left for the unit
+    # kernels (empty work list)
+    w = I.random_case(52, T=1000, lengths=[1000], n_adapters=1, ranks=[64], h_in=512, h_out=256)
+    y, Wh, word = run_layer(w)
+    assert word == 0
+    yr, st = oracle_delta(w, 0, None, W=Wh)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
