@@ -207,8 +207,10 @@ int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, 
 bool sgmv_shrink_ok(const lora_pool *pool, int h_in, int S);
 bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S);
 // plan: nullptr (items from the segment table) or a plan from launch_sgmv_plan
-// skip_fused: the plan's item masks name rows whose v the tensor-core shrink computes; items
-// all of whose rows are such rows are skipped.  tc_min_rows > 0 (segment tables): items of
+// skip_fused (with a layer plan that fuses M-tiles into the GEMM): the plan's shrink units, which
+// leave out the rows of those tiles (the tensor-core shrink computes their v), by persistent
+// clusters; the expand takes the plan's expand units when given tile_ad.  tc_min_rows > 0
+// (segment tables): items of
 // segments the tensor-core shrink takes (that many rows or more, rank kShrinkTcSegMinRank..kFuseMaxRank)
 // are skipped.
 int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *x, float *v, int ld_v,

@@ -167,7 +167,7 @@ struct Item {
     int a;
     int off;
     int nt;
-    int pad;    // plan with GEMM-fused tiles: bit k set when row k's term is added by the GEMM
+    int pad;    // segment tables: the segment's length
 };
 
 // A unit of the persistent shrink and expand kernels of a layer plan: one
@@ -219,8 +219,7 @@ __device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int 
 struct ItemSource {
     const int *seg_starts, *seg_adapter;
     int S, T;
-    const int *plan;     // nullptr, or [n_items, n_work, pad x2, perm[T], items[...] as Item, ...]
-    const Item *work;    // nullptr, or the plan's compacted items that still have rows to do (count plan[1])
+    const int *plan;     // nullptr, or a plan (see plan_layout): perm[T] and items[...] as Item
 };
 
 __device__ __forceinline__ const int *plan_perm(const int *plan) { return plan + 4; }
@@ -230,10 +229,6 @@ __device__ __forceinline__ const Item *plan_items(const int *plan, int T) {
 
 template <int NT>
 __device__ Item get_item(const ItemSource &src, int idx, int *scan, int *wtot) {
-    if (src.work) {       // both loads at once; an index past the count reads an unused slot and drops it
-        const Item it = src.work[idx];
-        return idx < src.plan[1] ? it : Item{-1, 0, 0, 0};
-    }
     if (src.plan) return plan_items(src.plan, src.T)[idx];   // idx < the plan's item bound; unused items have a = -1
     return segment_item<NT>(src.seg_starts, src.seg_adapter, src.S, src.T, idx, scan, wtot);
 }
@@ -269,7 +264,6 @@ struct PlanParams {
     int m;
     int *tile_ad;       // nullptr, or [n_tiles]: adapter whose term the GEMM adds for that M-tile, -1 if none
     int n_tiles;
-    Item *work;         // with tile_ad: compacted copies of the items that keep rows outside such tiles
     Unit *su, *eu;      // with tile_ad: shrink and expand units of the work items (counts plan[2], plan[3])
     int npc_s;          // ranks per shrink unit
     int nb_total;       // column blocks of kNb in h_out
@@ -411,7 +405,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     __syncthreads();
     // each item's mask of rows that sit in such tiles (the expand skips them;
     // the item's perm entries are read with independent loads); items that keep
-    // other rows go to the work list, one atomic per warp
+    // other rows get a work slot (one atomic per warp) and their unit counts
     const int nitems = min(n_items, p.max_items);
     for (int i0 = 0; i0 < nitems; i0 += kPlanThreads) {
         const int i = i0 + tid;
@@ -430,7 +424,6 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
                 for (int k = 0; k < kM; ++k)
                     if (tk[k] >= 0 && tk[k] < p.T && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0)
                         mask |= 1u << k;
-                items[i].pad = (int)mask;
                 const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
                 want = (mask & all) != all;        // rows left for the SGMV kernels (slot order is immaterial)
                 w = it;
@@ -443,7 +436,6 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         slot = __shfl_sync(0xffffffffu, slot, 0);
         if (want) {
             const int k = slot + __popc(bal & ((1u << lane) - 1u));
-            p.work[k] = w;
             if (p.su) {
                 // units of this item: 16-row halves that keep rows x rank chunks (shrink), column
                 // block ranges (expand); counted in the costly class or the cheap one
@@ -509,7 +501,6 @@ struct ShrinkParams {
     PoolView pv;
     ItemSource src;
     int m, h_in;
-    bool skip_fused;   // skip plan items whose rows all sit in tensor-core-shrunk tiles
     int tc_min_rows;   // > 0: skip segments of at least this many rows the tensor-core shrink takes
     int npc;       // ranks per CTA: max_rank rounded up to 16, at most 32 (64 in the wide kernel); grid.y covers the rest
     int alias_bytes;   // wide kernel: shared bytes of the ring / segment scan / partial sums (they alias)
@@ -651,10 +642,6 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
     const int row0 = blockIdx.z * kRowsS;
     const int nt = min(kRowsS, it.nt - row0);
     if (it.a < 0 || nt <= 0) return;
-    if (p.skip_fused && p.src.plan) {
-        const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
-        if (((unsigned)it.pad & all) == all) return;
-    }
     // the item's tokens load together with the record (load_record's barrier publishes both)
     if (tid < kRowsS)
         tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + row0 + tid] : it.off + row0 + tid, 0),
@@ -782,10 +769,6 @@ __global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkPa
     const Item it = get_item<kThreadsW>(p.src, blockIdx.x, scan, wtot);
     const int nt = min(kRowsW, it.nt);
     if (it.a < 0 || nt <= 0) return;
-    if (p.skip_fused && p.src.plan) {
-        const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
-        if (((unsigned)it.pad & all) == all) return;
-    }
     if (tid < kRowsW)
         tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
                             : 0;
@@ -943,7 +926,6 @@ struct ExpandParams {
     __nv_bfloat16 *y;
     int ncg;       // column groups per item
     int bpu;       // column blocks per unit (1 .. kMaxBlocksPerUnit)
-    const int *tile_ad;   // non-null: the plan's item masks name rows whose term the GEMM already added
     const Unit *units;    // unit kernel: the plan's expand units (count plan[3])
 };
 
@@ -1151,8 +1133,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
     const int cg = blockIdx.x % p.ncg;
     const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
     if (it.a < 0 || it.nt <= 0) return;
-    const unsigned fused = (p.tile_ad && p.src.plan) ? (unsigned)it.pad : 0u;
-    expand_unit(p, it, fused, cg * p.bpu, p.bpu, cg == 0, smem_raw);
+    expand_unit(p, it, 0u, cg * p.bpu, p.bpu, cg == 0, smem_raw);
 }
 
 // Layer plans: persistent CTAs walk the plan's expand units (costly ones first,
@@ -1186,11 +1167,11 @@ bool sgmv_expand_ok(const lora_pool *pool, int h_out, int S) {
 }
 
 // Plan layout in ints from its start: header [n_items, n_work, n_shrink_units,
-// n_expand_units], perm[T], items, M-tile adapters, work items, then (layer
-// plans) shrink and expand units.  Every array starts 16-byte aligned.
+// n_expand_units], perm[T], items, M-tile adapters, then (layer plans) shrink
+// and expand units.  Every array starts 16-byte aligned.
 struct PlanLayout {
     int max_items, max_su, max_eu;
-    size_t tiles, work, su, eu, total;   // offsets in ints; total bytes
+    size_t tiles, su, eu, total;   // offsets in ints; total bytes
 };
 
 // Ranks per shrink CTA of the 128-thread kernels.
@@ -1205,8 +1186,7 @@ static PlanLayout plan_layout(const lora_pool *pool, int matrix, int T) {
     L.max_su = L.max_items * 2 * ((pool->max_rank + shrink_npc(pool) - 1) / shrink_npc(pool));
     L.max_eu = L.max_items * ((std::max(0, pool->mat_h_out[matrix]) + kNb - 1) / kNb);
     L.tiles = 4 + (size_t)((T + 3) & ~3) + (size_t)L.max_items * item_ints;
-    L.work = L.tiles + (size_t)((n_tiles + 3) & ~3);
-    L.su = L.work + (size_t)L.max_items * item_ints;
+    L.su = L.tiles + (size_t)((n_tiles + 3) & ~3);
     L.eu = L.su + (size_t)L.max_su * item_ints;
     L.total = (L.eu + (size_t)L.max_eu * item_ints) * 4 + 64;
     return L;
@@ -1218,9 +1198,6 @@ int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan) {
     return plan + plan_layout(pool, matrix, T).tiles;
 }
 
-static Item *sgmv_plan_work(const lora_pool *pool, int matrix, int T, int *plan) {
-    return reinterpret_cast<Item *>(plan + plan_layout(pool, matrix, T).work);
-}
 
 // Shared memory of the plan kernel: the counting-sort area, the scan words and,
 // for layer plans, the unit-building arrays.
@@ -1253,7 +1230,6 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.m = matrix;
     p.tile_ad = tile_ad;
     p.n_tiles = (T + kTileRows - 1) / kTileRows;
-    p.work = tile_ad ? reinterpret_cast<Item *>(plan + L.work) : nullptr;
     p.su = tile_ad ? reinterpret_cast<Unit *>(plan + L.su) : nullptr;
     p.eu = tile_ad ? reinterpret_cast<Unit *>(plan + L.eu) : nullptr;
     p.npc_s = shrink_npc(pool);
@@ -1277,11 +1253,9 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
                        const int *seg_starts, const int *seg_adapter, int S, int T, const int *plan,
                        cudaStream_t st, bool skip_fused, int tc_min_rows) {
     ShrinkParams p;
-    p.skip_fused = skip_fused;
     p.tc_min_rows = tc_min_rows;
     p.pv = pool->view();
-    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan,
-                       skip_fused && plan ? sgmv_plan_work(pool, matrix, T, const_cast<int *>(plan)) : nullptr};
+    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
     p.m = matrix;
     p.h_in = h_in;
     p.x = static_cast<const __nv_bfloat16 *>(x);
@@ -1368,20 +1342,17 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
                        cudaStream_t st, const int *tile_ad) {
     ExpandParams p;
     p.pv = pool->view();
-    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan,
-                       tile_ad && plan ? sgmv_plan_work(pool, matrix, T, const_cast<int *>(plan)) : nullptr};
+    p.src = ItemSource{seg_starts, seg_adapter, S, T, plan};
     p.m = matrix;
     p.h_out = h_out;
     p.kpc = std::min(64, (pool->max_rank + 15) / 16 * 16);
     p.v = v;
     p.ld_v = ld_v;
     p.y = static_cast<__nv_bfloat16 *>(y);
-    p.tile_ad = tile_ad;
     const int nb_total = (h_out + kNb - 1) / kNb;
     // wide units amortise each unit's start-up latency (measured: fewer, longer
-    // CTAs win even when the grid is below the resident-CTA count); a plan's
-    // compacted work list (many tiny decode items) keeps narrower units
-    p.bpu = tile_ad ? 4 : kMaxBlocksPerUnit;
+    // CTAs win even when the grid is below the resident-CTA count)
+    p.bpu = kMaxBlocksPerUnit;
     p.ncg = (nb_total + p.bpu - 1) / p.bpu;
     const size_t smem = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
                         (size_t)(kM + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
