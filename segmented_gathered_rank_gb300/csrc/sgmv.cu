@@ -13,6 +13,14 @@
 // of a batch by adapter with a counting sort (so a decode batch whose tokens
 // are one-token segments still gets items of up to kM tokens).
 //
+// For the adapted layer the plan also marks the GEMM M-tiles whose rows share
+// one adapter (the GEMM adds their term itself) and lists, for the items that
+// keep other rows, work units ordered by cost: shrink units (a 16-row half x
+// a 32-rank chunk) and expand units (a range of column blocks, narrower for
+// costly items).  Persistent kernels walk these lists in snake order, the
+// shrink as clusters of two CTAs that split K and add their partial sums
+// through distributed shared memory.
+//
 // Adapter pages, x and y move with 16-byte asynchronous copies through
 // multi-stage shared-memory pipelines; the products run on the tensor cores
 // as warp-level mma.sync m16n8k16 (bf16 -> fp32) -- tiles here are 32
