@@ -88,15 +88,16 @@ KERNEL_SOURCES = {
 }
 
 
-def source_digest(workload: str | None = None) -> str:
+def source_digest(workload: str | None = None, csrc: str | None = None) -> str:
     """Digest of the kernel sources (those of `workload`'s dominant kernel, or
     all of them) with comments and blank lines removed, so that counters
     recorded for a kernel stay attached to it across comment edits and go
-    stale on any change of its code."""
+    stale on any change of its code.  csrc: the source folder (default: this
+    package's)."""
     import hashlib
     import re
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "segmented_gathered_rank_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "segmented_gathered_rank_gb300", "csrc")
     names = KERNEL_SOURCES.get(workload) if workload else None
     for n in sorted(os.listdir(csrc)):
         if n.endswith((".cu", ".cuh")) and (names is None or n in names):
