@@ -225,9 +225,13 @@ bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S, int T, bool units);
 size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T);
 // The plan's per-M-tile array (after its items).
 int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan);
-// tile_ad != nullptr: also classify the GEMM's 128-row M-tiles (see launch_gemm_tc).
+// tile_ad != nullptr (filled by launch_sgmv_tiles): also the fused rows' masks and the units.
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                     int *plan, cudaStream_t st, int *tile_ad = nullptr);
+                     int *plan, cudaStream_t st, const int *tile_ad = nullptr);
+// The fused M-tiles' adapters (see sgmv_tile_kernel) into tile_ad, the plan's per-M-tile array;
+// launch_sgmv_plan with that array must follow it in stream order.
+int launch_sgmv_tiles(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
+                      int *tile_ad, cudaStream_t st);
 int num_sms();   // SMs of the current device (cached)
 bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
 // tile_ad != nullptr: M-tiles with tile_ad[m] >= 0 also get that adapter's term

@@ -103,18 +103,22 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
     const bool tc = gemm_tc_ok(p, h_in, h_out, T);
     const bool tcs = tc && shrink_tc_ok(p, h_in, S);
     if (sgmv_plan_ok(p, matrix, S, T, tcs) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
-        // 1. plan: tokens grouped by adapter; GEMM M-tiles whose rows share one adapter
+        // 1. GEMM M-tiles whose rows share one adapter (tensor-core tiles)
         // 2. (tensor cores) v of those tiles: M 128 x N r contractions, K split over a cluster
-        // 3. v of every other adapted token (warp-MMA SGMV shrink)
-        // 4. base product; the uniform tiles add their low-rank term inside the GEMM
-        // 5. expand the remaining rows
-        // With tensor-core tiles, 3 reads only the plan and x and writes only v rows outside
-        // those tiles, which 2 and 4 never touch: it runs on a side stream beside them and
-        // joins before 5.
+        // 3. plan: the other rows' tokens grouped by adapter, as cost-ordered work units
+        // 4. v of every other adapted token (warp-MMA SGMV shrink)
+        // 5. base product; the uniform tiles add their low-rank term inside the GEMM
+        // 6. expand the remaining rows
+        // With tensor-core tiles, 3 and 4 read only the segment table, the tile flags and x
+        // and write only the plan and v rows outside those tiles, which 2 and 5 never touch:
+        // they run on a side stream beside them and join before 6.  Without, the plan
+        // comes first on the one stream.
         int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
                                             ~uintptr_t(255));
         int *tile_ad = tcs ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
-        if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, tile_ad))) return rc;
+        rc = tcs ? launch_sgmv_tiles(p, matrix, seg_starts, seg_adapter, S, T, tile_ad, st)
+                 : launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, nullptr);
+        if (rc) return rc;
         SideStream *side = tcs ? side_stream() : nullptr;
         if (side && cudaEventRecord(side->fork, st) != cudaSuccess) return LORA_ERR_CUDA;
         if (tcs && (rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, nullptr, nullptr, 0, v, p->max_rank, st)))
@@ -124,7 +128,10 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
             if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return LORA_ERR_CUDA;
             st3 = side->s;
         }
-        rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st3, tcs);
+        rc = tcs ? launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st3, tile_ad) : LORA_OK;
+        if (!rc)
+            rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st3,
+                                    tcs);
         if (side && cudaEventRecord(side->join, side->s) != cudaSuccess) return LORA_ERR_CUDA;
         if (rc) {
             if (side) cudaStreamWaitEvent(st, side->join, 0);     // no side work is left unjoined

@@ -270,7 +270,7 @@ struct PlanParams {
     int max_items;
     PoolView pv;        // for ranks of the tile classification
     int m;
-    int *tile_ad;       // nullptr, or [n_tiles]: adapter whose term the GEMM adds for that M-tile, -1 if none
+    const int *tile_ad; // nullptr, or [n_tiles] from sgmv_tile_kernel: the fused M-tiles' adapters, -1 if none
     int n_tiles;
     Unit *su, *eu;      // with tile_ad: shrink and expand units of the work items (counts plan[2], plan[3])
     int npc_s;          // ranks per shrink unit
@@ -279,6 +279,53 @@ struct PlanParams {
     int rank_cap;       // ranks beyond this are not computed (the v row length)
     int body;           // ints of the counting-sort area of shared memory
 };
+
+// GEMM M-tiles whose rows all use one adapter of rank 1..kFuseMaxRank: the
+// GEMM adds that adapter's term itself (and the tensor-core shrink computes
+// its v), so the plan leaves those rows out of its units.  One CTA: the
+// segment table in shared memory, a thread per tile.
+struct TileParams {
+    const int *seg_starts, *seg_adapter;
+    int S, T;
+    int n_ids;          // adapter ids below this may be loaded on the matrix
+    PoolView pv;
+    int m;
+    int *tile_ad;       // output [n_tiles]: the tile's adapter, -1 if the tile is not fused
+    int n_tiles;
+};
+
+__global__ void __launch_bounds__(kPlanThreads) sgmv_tile_kernel(TileParams p) {
+    extern __shared__ __align__(16) int sm[];
+    int *sb = sm;                        // [S + 1] segment bounds, clamped into [0, T]
+    int *sa = sb + p.S + 1;              // [S] segment adapters (-1: none or invalid)
+    for (int s = threadIdx.x; s <= p.S; s += kPlanThreads) sb[s] = min(max(p.seg_starts[s], 0), p.T);
+    for (int s = threadIdx.x; s < p.S; s += kPlanThreads) {
+        const int a = p.seg_adapter[s];
+        sa[s] = a < p.n_ids ? a : -1;
+    }
+    __syncthreads();
+    for (int mb = threadIdx.x; mb < p.n_tiles; mb += kPlanThreads) {
+        const int r0 = mb * kTileRows, r1 = min(p.T, r0 + kTileRows);
+        int lo = 0, hi = p.S;                   // first segment bound above r0
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sb[mid] > r0) hi = mid; else lo = mid + 1;
+        }
+        int a = -2;
+        bool uniform = true;
+        for (int s = max(lo - 1, 0); s < p.S && sb[s] < r1 && uniform; ++s) {
+            if (sb[s + 1] <= sb[s]) continue;
+            if (a == -2) a = sa[s];
+            else if (sa[s] != a) uniform = false;
+        }
+        int out = -1;
+        if (uniform && a >= 0 && a < p.n_ids) {
+            const int rank = p.pv.table[((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints];
+            if (rank >= 1 && rank <= kFuseMaxRank) out = a;
+        }
+        p.tile_ad[mb] = out;
+    }
+}
 
 // Column blocks per expand unit from an item's cost per block: its y rows,
 // read and written once per pass of up to 32 ranks, plus its B rows.
@@ -381,35 +428,13 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     if (!p.tile_ad) return;
     int *wcount = wtot + nwarps + 1;        // past block_scan's words
     if (tid == 0) *wcount = 0;
-    // GEMM M-tiles whose rows all use one adapter of rank 1..kFuseMaxRank: the
-    // GEMM adds that adapter's term itself, and the expand skips those rows.
-    // The flags are also kept in shared memory (in the counters' space, free
-    // by now) when they fit there.
+    // the GEMM-fused M-tiles (sgmv_tile_kernel's flags), kept in shared memory
+    // (in the counters' space, free by now) when they fit there
     __syncthreads();
     int *tflag = cnt;
     const bool staged = p.n_tiles <= 3 * p.n_ids + p.S;
-    for (int mb = tid; mb < p.n_tiles; mb += kPlanThreads) {
-        const int r0 = mb * kTileRows, r1 = min(p.T, r0 + kTileRows);
-        int lo = 0, hi = p.S;                   // first segment bound above r0
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sb[mid] > r0) hi = mid; else lo = mid + 1;
-        }
-        int a = -2;
-        bool uniform = true;
-        for (int s = max(lo - 1, 0); s < p.S && sb[s] < r1 && uniform; ++s) {
-            if (sb[s + 1] <= sb[s]) continue;
-            if (a == -2) a = sa[s];
-            else if (sa[s] != a) uniform = false;
-        }
-        int out = -1;
-        if (uniform && a >= 0 && a < p.n_ids) {
-            const int rank = arank[a];
-            if (rank >= 1 && rank <= kFuseMaxRank) out = a;
-        }
-        p.tile_ad[mb] = out;
-        if (staged) tflag[mb] = out;
-    }
+    if (staged)
+        for (int mb = tid; mb < p.n_tiles; mb += kPlanThreads) tflag[mb] = p.tile_ad[mb];
     __syncthreads();
     // each item's mask of rows that sit in such tiles (the expand skips them;
     // the item's perm entries are read with independent loads); items that keep
@@ -1222,8 +1247,33 @@ bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S, int T, bool units) {
     return pool->mat_n_ids[matrix] > 0 && S <= kMaxS && plan_smem(pool, matrix, S, T, units, &body) <= 160 * 1024;
 }
 
+int launch_sgmv_tiles(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
+                      int *tile_ad, cudaStream_t st) {
+    TileParams p;
+    p.seg_starts = seg_starts;
+    p.seg_adapter = seg_adapter;
+    p.S = S;
+    p.T = T;
+    p.n_ids = pool->mat_n_ids[matrix];
+    p.pv = pool->view();
+    p.m = matrix;
+    p.tile_ad = tile_ad;
+    p.n_tiles = (T + kTileRows - 1) / kTileRows;
+    const size_t smem = (size_t)(2 * S + 1) * 4;
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(sgmv_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        configured = smem;
+    }
+    sgmv_tile_kernel<<<1, kPlanThreads, smem, st>>>(p);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                     int *plan, cudaStream_t st, int *tile_ad) {
+                     int *plan, cudaStream_t st, const int *tile_ad) {
     const PlanLayout L = plan_layout(pool, matrix, T);
     PlanParams p;
     p.seg_starts = seg_starts;
