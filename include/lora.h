@@ -174,8 +174,8 @@ size_t lora_layer_forward_workspace_size(const lora_pool *pool, int matrix, int 
  * adapter (or with an invalid one) get the base term only.
  * workspace: device scratch of at least lora_layer_forward_workspace_size()
  * bytes, owned by the caller, contents undefined on entry and exit.
- * Streams: part of the call's work (the shrink of rows whose M-tile is not
- * fused into the GEMM) may run on an internal stream, one per host thread
+ * Streams: part of the call's work (planning the rows whose M-tile is not
+ * fused into the GEMM, and their shrink) may run on an internal stream, one per host thread
  * and device, that the call forks from `stream` and joins back to it with
  * events; the call's work as a whole stays ordered after earlier work on
  * `stream` and before later work on it, and under stream capture the fork
