@@ -7,7 +7,11 @@ Metric: adapted tokens/s per LoRA layer -- tokens that pass through one
 adapted projection per second (a step over L projections of T tokens counts
 T * L).  Rank 0 prints one JSON line.
 
-Workloads (``--workload``; default ``decode_bgmv``):
+Workloads (``--workload``; default ``fused_layer``):
+  fused_layer         4 x 1024 prefill + 512 decode tokens; a step is
+                      lora_layer_forward on q, k, v, o (base GEMM + adapter),
+                      Llama-3-8B shapes -- the largest workload, and the one
+                      whose base product is a tensor-core contraction.
   decode_bgmv         256 decode tokens, ids uniform over 32 adapters, 4096->4096,
                       rank 16, bf16.  A step is one decode pass through 32
                       layers' adapted q projection: 32 lora_bgmv launches, each
@@ -16,8 +20,9 @@ Workloads (``--workload``; default ``decode_bgmv``):
                       expand on q, k, v, o.
   encoder_mixed_rank  16384 tokens (128 x 128), 1024 adapters of ranks 8..64,
                       a step is shrink + expand on all 48 projections.
-  fused_layer         4 x 1024 prefill + 512 decode tokens; a step is
-                      lora_layer_forward on q, k, v, o (base GEMM + adapter).
+
+The prefill and encoder lines carry a second roofline object,
+``shrink_roofline``, for the shrink kernel (the expand is the first).
 
 Each step is captured once in a CUDA graph and replayed; the timed region is
 bracketed by a barrier and a device synchronise on both sides and measured
@@ -79,12 +84,17 @@ def load_traffic():
         return {}
 
 
-# The sources each workload's dominant kernel is built from: its recorded
-# DRAM traffic stays valid while these are unchanged.
+# The sources each recorded kernel (a workload's dominant kernel, or a
+# "<workload>.<kernel>" secondary one) is built from: its recorded DRAM
+# traffic stays valid while these are unchanged.  The fused layer's unit is a
+# whole multi-kernel call, so every source counts (None).
 KERNEL_SOURCES = {
     "decode_bgmv": ("bgmv.cu", "internal.cuh"),
     "prefill_sgmv": ("sgmv.cu", "internal.cuh"),
+    "prefill_sgmv.shrink": ("sgmv.cu", "internal.cuh"),
     "encoder_mixed_rank": ("sgmv.cu", "internal.cuh"),
+    "encoder_mixed_rank.shrink": ("sgmv.cu", "internal.cuh"),
+    "fused_layer": None,
 }
 
 
@@ -232,6 +242,11 @@ class Runner:
         """Launches of the dominant kernel for one step (default: the step)."""
         self.step(stream)
 
+    # other kernels reported with a roofline of their own: key -> (spec like
+    # `dominant`, function launching that kernel's calls of one step)
+    def secondary(self):
+        return {}
+
 
 class DecodeBGMV(Runner):
     name = "decode_bgmv"
@@ -356,6 +371,17 @@ class PrefillSGMV(Runner):
             L.lora_sgmv_expand(self.pool.handle, m, self.v[m], w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T,
                                stream)
 
+    def shrink_step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(4):
+            L.lora_sgmv_shrink(self.pool.handle, m, self._x(m), self.v[m], w.max_rank, self.ss, self.sa, w.S, w.T,
+                               stream)
+
+    def secondary(self):
+        spec = dict(name="lora_sgmv_shrink", bound="hbm", work_per_launch=sum(self.shrink_b) / 4,
+                    launches_per_step=4, unit="GB/s", traffic_key="prefill_sgmv.shrink")
+        return {"shrink_roofline": (spec, self.shrink_step)}
+
     def e2e_setup(self):
         self.x_h = {k: v.cpu().pin_memory() for k, v in self.x.items()}
         self.y_h = [y.cpu().pin_memory() for y in self.y]
@@ -419,6 +445,7 @@ class EncoderMixedRank(Runner):
         tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
         eb = A.expand_bytes(tok, w.ranks, 768, 2)
         sb = A.shrink_bytes(tok, w.ranks, 768, 2, w.max_rank)
+        self.shrink_bytes = sb
         self.dominant = dict(name="lora_sgmv_expand", bound="hbm", work_per_launch=eb, launches_per_step=self.M,
                              unit="GB/s")
         self.config = {"workload": self.describe(),
@@ -436,6 +463,16 @@ class EncoderMixedRank(Runner):
         w, L = self.w, self.L
         for m in range(self.M):
             L.lora_sgmv_expand(self.pool.handle, m, self.v, w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T, stream)
+
+    def shrink_step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(self.M):
+            L.lora_sgmv_shrink(self.pool.handle, m, self.x[m], self.v, w.max_rank, self.ss, self.sa, w.S, w.T, stream)
+
+    def secondary(self):
+        spec = dict(name="lora_sgmv_shrink", bound="hbm", work_per_launch=self.shrink_bytes, launches_per_step=self.M,
+                    unit="GB/s", traffic_key="encoder_mixed_rank.shrink")
+        return {"shrink_roofline": (spec, self.shrink_step)}
 
     def e2e_setup(self):
         self.x_h = [t.cpu().pin_memory() for t in self.x]
@@ -649,28 +686,41 @@ def run_ours(args, dist: Dist):
     value, t_max = aggregate(runner.units_per_step, args.steps, t_local, dist)
     ms_per_step = 1e3 * t_max / args.steps
 
-    # Dominant kernel: its launches alone, replayed over the same number of steps.
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        d0.record(stream)
-        for _ in range(args.steps):
-            g_dom.replay()
-        d1.record(stream)
-    torch.cuda.synchronize()
-    dom = runner.dominant
-    per_launch_s = d0.elapsed_time(d1) / 1e3 / (args.steps * dom["launches_per_step"])
+    # Dominant kernel (and any secondary one): its launches alone, replayed
+    # over the same number of steps, timed on the launching stream.
     peaks, peak_src = load_peaks()
-    if dom["bound"] == "hbm":
-        achieved = dom["work_per_launch"] / per_launch_s / 1e9
-        peak = peaks["hbm_gbs"]
-    else:
-        achieved = dom["work_per_launch"] / per_launch_s / 1e12
-        peak = peaks["bf16_tflops"]
-    traffic_rec = load_traffic().get(args.workload)
-    traffic = None
-    if traffic_rec and traffic_rec.get("source_digest") == source_digest(args.workload):
-        traffic = traffic_rec.get("dram_bytes_per_launch")
+    traffic_db = load_traffic()
+
+    def roofline(spec, graph, key):
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            d0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
+        per_launch_s = d0.elapsed_time(d1) / 1e3 / (args.steps * spec["launches_per_step"])
+        if spec["bound"] == "hbm":
+            achieved = spec["work_per_launch"] / per_launch_s / 1e9
+            peak = peaks["hbm_gbs"]
+        else:
+            achieved = spec["work_per_launch"] / per_launch_s / 1e12
+            peak = peaks["bf16_tflops"]
+        rec = traffic_db.get(key)
+        traffic = None
+        if rec and rec.get("source_digest") == source_digest(key):
+            traffic = rec.get("dram_bytes_per_launch")
+        return {"bound": spec["bound"], "achieved": achieved, "peak": peak, "unit": spec["unit"],
+                "frac": achieved / peak, "traffic": traffic, "kernel": spec["name"],
+                "work_per_launch": spec["work_per_launch"], "launch_us": per_launch_s * 1e6,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src}
+
+    roof = roofline(runner.dominant, g_dom, args.workload)
+    extra = {}
+    for name, (spec, fn) in runner.secondary().items():
+        g2, _ = capture(fn)
+        extra[name] = roofline(spec, g2, spec.get("traffic_key", name))
 
     # End to end through the public API with host buffers.
     runner.e2e_setup()
@@ -700,10 +750,8 @@ def run_ours(args, dist: Dist):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
             "config": {**runner.config, "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single"},
-            "roofline": {"bound": dom["bound"], "achieved": achieved, "peak": peak, "unit": dom["unit"],
-                         "frac": achieved / peak, "traffic": traffic, "kernel": dom["name"],
-                         "work_per_launch": dom["work_per_launch"], "launch_us": per_launch_s * 1e6,
-                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src},
+            "roofline": roof,
+            **extra,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(runner.h2d),
                     "d2h_bytes_per_step": int(runner.d2h)},
@@ -720,7 +768,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="decode_bgmv", choices=sorted(RUNNERS))
+    ap.add_argument("--workload", default="fused_layer", choices=sorted(RUNNERS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--ref-step-seconds", type=float, default=1.0, help="reference-arm work per step")

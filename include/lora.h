@@ -231,6 +231,45 @@ const char *lora_strerror(int status);
  * not counted again). */
 unsigned long long lora_launch_count(void);
 
+/*
+ * Two-tier adapter residency cache (host code; no device access).
+ *
+ * "Multi-LoRA Serving - S-LoRA/Punica Batching, Adapter Hot-Swap & Memory",
+ * section "Memory: slots, tiers and paging" and its adapter-cache simulation:
+ * a few GPU slots (here: adapters resident in the paged pool), backed by a
+ * larger host-RAM tier, backed by disk.  Each tier keeps its adapters in
+ * least-recently-used order and evicts the least recently used one when a
+ * new one would exceed its slot count.  A request first looks in the GPU
+ * tier; only on a GPU miss is the host tier looked up (and reordered).  A
+ * slot count of 0 keeps nothing.
+ *
+ * The cache decides residency only and moves no data: a caller maps a GPU
+ * hit to "already in the pool", a host hit to an upload from pinned host
+ * memory (lora_pool_load_async), a disk hit to a fetch plus that upload, and
+ * the GPU tier's eviction to lora_pool_unload_async.
+ */
+typedef struct lora_tier_cache lora_tier_cache;
+enum { LORA_TIER_GPU = 0, LORA_TIER_HOST = 1, LORA_TIER_DISK = 2 };
+
+/* Adapter ids 0..n_keys-1; both tiers start empty.  Errors: LORA_ERR_ARG. */
+int lora_tier_cache_create(lora_tier_cache **out, int n_keys, int gpu_slots, int host_slots);
+int lora_tier_cache_destroy(lora_tier_cache *cache);   /* NULL accepted */
+
+/* One request for `adapter`: returns the tier that served it (LORA_TIER_*),
+ * or LORA_ERR_ARG for an id out of range.  *gpu_evicted (may be NULL) gets
+ * the adapter the GPU tier dropped to make room, or -1. */
+int lora_tier_cache_touch(lora_tier_cache *cache, int adapter, int *gpu_evicted);
+
+/* Bit 0: the adapter is in the GPU tier; bit 1: in the host tier.
+ * LORA_ERR_ARG for an id out of range. */
+int lora_tier_cache_resident(const lora_tier_cache *cache, int adapter);
+
+/* Replays a request trace (adapter ids in 0..n_keys-1) through a fresh
+ * cache: counts[0] GPU hits, counts[1] host hits, counts[2] disk loads.
+ * Errors: LORA_ERR_ARG (NULL, n < 0, an id out of range). */
+int lora_tier_sim(const int *trace, long long n, int n_keys, int gpu_slots, int host_slots,
+                  long long *counts);
+
 #ifdef __cplusplus
 }
 #endif

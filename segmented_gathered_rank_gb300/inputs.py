@@ -149,6 +149,7 @@ class Workload:
     shared_x: dict = field(default_factory=dict)   # matrix index -> activation stream id
     layers: int = 1                                  # distinct copies (bench rotation)
     probe: bool = False                              # small-integer values (see integer_probe)
+    zero_b: tuple = ()                               # adapters whose B is all zeros (A_T drawn as usual)
 
     # -- tensors ----------------------------------------------------------
     def x(self, m: int = 0, layer: int = 0) -> np.ndarray:
@@ -182,10 +183,13 @@ class Workload:
         mat = self.matrices[m]
         r = int(self.ranks[a])
         if self.probe:
-            return probe_adapter(self.seed + 1000 * layer + m, a, r, mat.h_in, mat.h_out)
-        rng = _rng(self.seed, _K_ADAPTER, layer, m, a)
-        at = _store(self.a_dist.draw(rng, (r, mat.h_in)), self.dtype)
-        b = _store(self.b_dist.draw(rng, (r, mat.h_out)), self.dtype)
+            at, b = probe_adapter(self.seed + 1000 * layer + m, a, r, mat.h_in, mat.h_out)
+        else:
+            rng = _rng(self.seed, _K_ADAPTER, layer, m, a)
+            at = _store(self.a_dist.draw(rng, (r, mat.h_in)), self.dtype)
+            b = _store(self.b_dist.draw(rng, (r, mat.h_out)), self.dtype)
+        if a in self.zero_b:
+            b = np.zeros_like(b)
         return at, b
 
     @property
@@ -212,6 +216,42 @@ def bounded_zipf(rng: np.random.Generator, n: int, s: float, size: int) -> np.nd
     cdf = np.cumsum(w / w.sum())
     u = rng.random(size)
     return np.minimum(np.searchsorted(cdf, u, side="left"), n - 1).astype(np.int32)
+
+
+def lcg_uniforms(seed: int, n: int) -> np.ndarray:
+    """The linear congruential generator of the adapter-cache simulation on
+    "Multi-LoRA Serving" (section "Memory: slots, tiers and paging"): state
+    s <- (1664525 s + 1013904223) mod 2^32 starting from ``seed``, each step
+    yielding s / 2^32 in [0, 1).  Exact integer arithmetic."""
+    out = np.empty(n, np.float64)
+    s = seed & 0xFFFFFFFF
+    for i in range(n):
+        s = (s * 1664525 + 1013904223) & 0xFFFFFFFF
+        out[i] = s / 4294967296.0
+    return out
+
+
+def adapter_request_trace(n_adapters: int = 500, requests: int = 50_000, s: float = 1.1,
+                          seed: int = 11) -> np.ndarray:
+    """Adapter ids of a request stream with Zipf(s) popularity, drawn as the
+    page's adapter-cache simulation draws them: weights 1 / (i+1)^s for ids
+    i = 0..n-1, a cumulative distribution built by adding the normalised
+    weights left to right (the total itself summed left to right), and for
+    each LCG uniform u the first id whose cumulative value is >= u.  The
+    defaults are that simulation's workload (500 adapters, 50,000 requests,
+    s = 1.1, LCG seed 11)."""
+    w = [1.0 / float(i + 1) ** s for i in range(n_adapters)]
+    total = 0.0
+    for v in w:
+        total += v
+    cdf = np.empty(n_adapters, np.float64)
+    acc = 0.0
+    for i, v in enumerate(w):
+        acc = acc + v / total
+        cdf[i] = acc
+    u = lcg_uniforms(seed, requests)
+    ids = np.searchsorted(cdf, u, side="left")
+    return np.minimum(ids, n_adapters - 1).astype(np.int32)
 
 
 def zipf_lengths(n: int, s: float, total: int, cap: int) -> np.ndarray:

@@ -34,10 +34,15 @@ LORA_DEV_WAIT_TIMEOUT = 4
 
 LORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
+LORA_TIER_GPU = 0
+LORA_TIER_HOST = 1
+LORA_TIER_DISK = 2
+
 EXPORTS = ["lora_pool_create", "lora_pool_destroy", "lora_pool_load", "lora_pool_unload",
            "lora_pool_free_pages", "lora_sgmv_shrink", "lora_sgmv_expand", "lora_bgmv",
            "lora_layer_forward_workspace_size", "lora_layer_forward", "lora_get_error", "lora_strerror",
-           "lora_launch_count", "lora_layer_forward_noalloc"]
+           "lora_launch_count", "lora_layer_forward_noalloc", "lora_tier_cache_create", "lora_tier_cache_destroy",
+           "lora_tier_cache_touch", "lora_tier_cache_resident", "lora_tier_sim"]
 
 if not os.path.exists(_build.LIB):
     raise ImportError(f"CUDA library {_build.LIB} is not built: run segmented_gathered_rank_gb300.build.build()")
@@ -70,6 +75,11 @@ _sig("lora_layer_forward_noalloc", _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P)
 _sig("lora_get_error", _I, _P, ctypes.POINTER(_I))
 _sig("lora_strerror", ctypes.c_char_p, _I)
 _sig("lora_launch_count", ctypes.c_ulonglong)
+_sig("lora_tier_cache_create", _I, ctypes.POINTER(_P), _I, _I, _I)
+_sig("lora_tier_cache_destroy", _I, _P)
+_sig("lora_tier_cache_touch", _I, _P, _I, ctypes.POINTER(_I))
+_sig("lora_tier_cache_resident", _I, _P, _I)
+_sig("lora_tier_sim", _I, _P, ctypes.c_longlong, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong))
 
 
 class LoraError(RuntimeError):
@@ -194,3 +204,39 @@ def lora_get_error(pool) -> tuple[int, int]:
     word = ctypes.c_int(0)
     rc = _lib.lora_get_error(pool, ctypes.byref(word))
     return int(rc), int(word.value)
+
+
+def lora_tier_cache_create(n_keys: int, gpu_slots: int, host_slots: int) -> int:
+    """Two-tier LRU residency cache (host only); returns its handle."""
+    h = ctypes.c_void_p()
+    _check(_lib.lora_tier_cache_create(ctypes.byref(h), n_keys, gpu_slots, host_slots), "lora_tier_cache_create")
+    return h.value
+
+
+def lora_tier_cache_destroy(cache) -> None:
+    _check(_lib.lora_tier_cache_destroy(cache), "lora_tier_cache_destroy")
+
+
+def lora_tier_cache_touch(cache, adapter: int) -> tuple[int, int]:
+    """(tier that served the request, adapter the GPU tier evicted or -1)."""
+    ev = ctypes.c_int(-1)
+    rc = _lib.lora_tier_cache_touch(cache, adapter, ctypes.byref(ev))
+    if rc < 0:
+        raise LoraError(rc, "lora_tier_cache_touch")
+    return int(rc), int(ev.value)
+
+
+def lora_tier_cache_resident(cache, adapter: int) -> int:
+    rc = _lib.lora_tier_cache_resident(cache, adapter)
+    if rc < 0:
+        raise LoraError(rc, "lora_tier_cache_resident")
+    return int(rc)
+
+
+def lora_tier_sim(trace, n_keys: int, gpu_slots: int, host_slots: int) -> tuple[int, int, int]:
+    """(GPU hits, host hits, disk loads) of a request trace (int32 host array)."""
+    tr = np.ascontiguousarray(trace, np.int32)
+    counts = (ctypes.c_longlong * 3)()
+    _check(_lib.lora_tier_sim(ctypes.c_void_p(tr.ctypes.data), len(tr), n_keys, gpu_slots, host_slots, counts),
+           "lora_tier_sim")
+    return int(counts[0]), int(counts[1]), int(counts[2])

@@ -1,9 +1,11 @@
 """GPU parity: every entry point against the CPU oracle on seeded inputs.
 
-Covers the five workloads at full size (the fused layer on sampled rows),
-small randomized ragged cases, integer probes compared bit for bit, and the
-edge cases (empty segments, tokens without an adapter, invalid ids, bad
-segment tables, rank 0, T = 0, pool exhaustion and page reuse).
+Covers the five workloads at full size (the fused layer on sampled rows of
+q and o, and on every row of k), small randomized ragged cases, integer
+probes compared bit for bit, and the edge cases: empty segments, tokens
+without an adapter, invalid ids, bad segment tables, rank-0 and zero-B
+adapters computed through every entry point (their rows keep the base or y0
+output bit for bit), T = 0, pool exhaustion and page reuse.
 """
 import numpy as np
 import pytest
@@ -156,6 +158,18 @@ def test_fused_layer_sampled(m):
     yr, st = oracle_delta(w, m, None, rows=rows, W=Wh)
     assert st == 0
     assert rel_err(y[rows], yr) <= TOL_Y[w.dtype]
+
+
+def test_fused_layer_k_every_row():
+    """The k projection (4096 -> 1024) of the fused workload on all 4608 rows:
+    every M-tile of the GEMM, every decode row and the rank-128 adapter's rows
+    are compared, so a scheduling slip confined to some rows cannot hide."""
+    w = I.fused_layer()
+    y, Wh, word = run_layer(w, 1)
+    assert word == 0 and not np.isnan(y).any()
+    yr, st = oracle_delta(w, 1, None, W=Wh)
+    assert st == 0
+    assert rel_err(y, yr) <= TOL_Y[w.dtype]
 
 
 def test_fused_layer_delta_alone():
@@ -457,3 +471,100 @@ def test_layer_one_segment_every_tile_fused():
     assert word == 0
     yr, st = oracle_delta(w, 0, None, W=Wh)
     assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+
+
+# ---------------------------------------------------------------------------
+# Rank-0 and zero-B adapters.  Their merged weight is W itself (S-LoRA slide 5,
+# W' = W + AB with AB = 0), so their rows must come out as the base product
+# (layer) or as y0 (SGMV, BGMV), bit for bit, while the other rows of the same
+# batch still match the oracle.  The batch gives the rank-0 adapter two whole
+# 128-row M-tiles and the zero-B adapter one (the GEMM's tile flags and its
+# fused adapter rounds see them), plus one-token segments of both mixed with
+# ordinary adapters (the plan's work units and the expand).
+# ---------------------------------------------------------------------------
+_DEGEN_RANKS = [16, 0, 128, 16, 8]      # adapter 1: rank 0; adapter 3: B = 0
+_DEGEN_ZERO_B = (3,)
+_DEGEN_IDS = (1, 3, 2)                  # the three whole tiles
+
+
+def _degenerate_case(seed, dtype=I.BF16, decode=False):
+    ragged = [37, 1, 1, 1, 90, 1, 1, 0, 64, 1, 1, 1, 13, 1, 1, 200, 1, 1, 1, 1]
+    ragged_ids = [1, 3, 0, 4, 2, -1, 1, 3, 3, 1, 0, 2, 4, 3, 1, 1, 2, 3, 0, 1]
+    lengths = [256, 128, 128] + ragged
+    T = int(sum(lengths))
+    w = I.random_case(seed, T=T, lengths=lengths, h_in=512, h_out=256, ranks=_DEGEN_RANKS, dtype=dtype)
+    w.seg_adapter = np.array(list(_DEGEN_IDS) + ragged_ids, np.int32)
+    w.zero_b = _DEGEN_ZERO_B
+    if decode:
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+        w.seg_starts = np.arange(T + 1, dtype=np.int32)
+        w.seg_adapter = tok.copy()
+        w.token_adapter = tok
+    return w
+
+
+def _degenerate_rows(w):
+    tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
+    keep = (tok == 1) | (tok == 3) | (tok < 0)
+    assert keep.sum() > 384 and (~keep).sum() > 200
+    return keep
+
+
+@pytest.mark.parametrize("dtype", [I.BF16, I.F32])
+def test_rank0_and_zero_b_sgmv(dtype):
+    w = _degenerate_case(61, dtype)
+    keep = _degenerate_rows(w)
+    v, y, y0, word = run_sgmv(w)
+    assert word == 0
+    yh0 = H.to_host(H.to_device(y0, w.dtype))
+    assert np.array_equal(y[keep], yh0[keep])
+    yr, st = oracle_delta(w, 0, y0)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+    vr, _ = oracle_v(w, 0, w.max_rank)
+    mask = written_mask(w, w.max_rank)
+    assert rel_err(v[mask], vr[mask]) <= TOL_V[w.dtype]
+
+
+@pytest.mark.parametrize("dtype", [I.BF16, I.F32])
+def test_rank0_and_zero_b_bgmv(dtype):
+    w = _degenerate_case(62, dtype, decode=True)
+    keep = _degenerate_rows(w)
+    y, y0, word = run_bgmv(w)
+    assert word == 0
+    yh0 = H.to_host(H.to_device(y0, w.dtype))
+    assert np.array_equal(y[keep], yh0[keep])
+    yr, st = oracle_delta(w, 0, y0)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+
+
+@pytest.mark.parametrize("dtype", [I.BF16, I.F32])
+def test_rank0_and_zero_b_layer(dtype):
+    w = _degenerate_case(63, dtype)
+    keep = _degenerate_rows(w)
+    y, Wh, word = run_layer(w)
+    assert word == 0 and not np.isnan(y).any()
+    yr, st = oracle_delta(w, 0, None, W=Wh)
+    assert st == 0 and rel_err(y, yr) <= TOL_Y[w.dtype]
+    # the same batch with no adapter at all: the base product alone
+    import dataclasses
+    wb = dataclasses.replace(w, seg_adapter=np.full_like(w.seg_adapter, -1))
+    y_base, _, word = run_layer(wb)
+    assert word == 0
+    assert np.array_equal(y[keep], y_base[keep])
+    # delta alone (W = 0): those rows are exactly zero
+    yd, _, word = run_layer(w, zero_w=True)
+    assert word == 0
+    assert np.array_equal(yd[keep], np.zeros_like(yd[keep]))
+    ydr, _ = oracle_delta(w, 0, None)
+    assert rel_err(yd, ydr) <= TOL_Y[w.dtype]
+
+
+def test_rank0_and_zero_b_decode_layer():
+    """One-token segments only: every row goes through the plan's units."""
+    w = _degenerate_case(64, I.BF16, decode=True)
+    keep = _degenerate_rows(w)
+    yd, _, word = run_layer(w, zero_w=True)
+    assert word == 0
+    assert np.array_equal(yd[keep], np.zeros_like(yd[keep]))
+    ydr, st = oracle_delta(w, 0, None)
+    assert st == 0 and rel_err(yd, ydr) <= TOL_Y[w.dtype]

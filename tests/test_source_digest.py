@@ -33,14 +33,19 @@ def test_digest_ignores_comments_and_blank_lines(tmp_path):
 
 def test_code_change_stales_only_the_workloads_built_from_that_file(tmp_path):
     d = _copy(tmp_path)
-    before = {w: bench.source_digest(w, d) for w in bench.KERNEL_SOURCES}
+    single = [w for w, names in bench.KERNEL_SOURCES.items() if names is not None]
+    before = {w: bench.source_digest(w, d) for w in single}
     all_before = bench.source_digest(None, d)
+    fused_before = bench.source_digest("fused_layer", d)
+    assert fused_before == all_before      # the fused layer's unit is a call over every kernel
     _edit(d, "layer_tc.cu", None, "\nstatic int unused_marker_for_the_test = 1;\n")
-    assert {w: bench.source_digest(w, d) for w in bench.KERNEL_SOURCES} == before   # no dominant kernel there
+    assert {w: bench.source_digest(w, d) for w in single} == before   # no single-kernel record there
     assert bench.source_digest(None, d) != all_before
+    assert bench.source_digest("fused_layer", d) != fused_before
     _edit(d, "sgmv.cu", None, "\nstatic int another_marker = 2;\n")
-    after = {w: bench.source_digest(w, d) for w in bench.KERNEL_SOURCES}
+    after = {w: bench.source_digest(w, d) for w in single}
     assert after["decode_bgmv"] == before["decode_bgmv"]
     assert after["prefill_sgmv"] != before["prefill_sgmv"]
     assert after["encoder_mixed_rank"] != before["encoder_mixed_rank"]
+    assert after["prefill_sgmv.shrink"] != before["prefill_sgmv.shrink"]
 
