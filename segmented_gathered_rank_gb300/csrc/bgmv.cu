@@ -418,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
     }
     item = mine;
     const int ia = item->a, intok = min(max(item->ntok, 0), kTok);
-    if (ia < 0 || intok == 0 || item->rank < 0) {
-        if (ia >= 0 && intok > 0 && crank == 0 && tid == 0) flag(pv.status, LORA_DEV_BAD_ADAPTER);
+    // nothing to add: no adapter, no tokens, or rank 0 (y stays as it is; an
+    // unloaded adapter is also flagged)
+    if (ia < 0 || intok == 0 || item->rank <= 0) {
+        if (ia >= 0 && intok > 0 && item->rank < 0 && crank == 0 && tid == 0) flag(pv.status, LORA_DEV_BAD_ADAPTER);
         asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
         cp_async_wait_all();   // no copy may still be landing when the CTA exits
         return;
@@ -585,13 +587,7 @@ int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, 
     const size_t smem = (size_t)lay.a_bytes + (size_t)kJ * (p.slice_out + 8) * 2 + (size_t)lay.xy_bytes +
                         (size_t)2 * kTok * kVPitch * 2 + (size_t)kC * kTok * kJ * 4 + 16 +
                         (size_t)(p.pv.rec_ints + kWarps + 2) * 4 + sizeof(Item) + 16;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(bgmv_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = smem;
-    }
+    if (smem_optin(reinterpret_cast<const void *>(bgmv_cluster_kernel), smem)) return LORA_ERR_CUDA;
     const int items = n_ids + (T + kTok - 1) / kTok;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(items * kC);

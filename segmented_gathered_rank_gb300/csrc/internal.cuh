@@ -184,6 +184,46 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// The adapter whose term the tensor-core GEMM adds itself for the M-tile of
+// rows [r0, r1): the one adapter every non-empty segment overlapping the tile
+// uses, or -1 when the tile mixes adapters, has a token without an adapter
+// (id < 0), or names an id >= n_ids (never loaded on the matrix).  sb: the S+1
+// segment bounds clamped into [0, T]; sa: the S segment adapters.  The caller
+// still checks the adapter's rank (1 .. kFuseMaxRank).  Segments are visited
+// from the one holding r0 onwards, stopping at the first bound >= r1, 32 at a
+// time by one warp (all 32 lanes call it and get the result).  The
+// tensor-core shrink (its own tile) and the rows / plan kernels (every tile)
+// decide with this one function on the same table, so they agree.
+__device__ __forceinline__ int uniform_tile_adapter(const int *sb, const int *sa, int S, int n_ids, int r0, int r1) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = S;                     // first segment bound above r0
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sb[mid] > r0) hi = mid; else lo = mid + 1;
+    }
+    int a = -1;
+    bool have = false, uniform = true;
+    for (int base = lo > 0 ? lo - 1 : 0; base < S; base += 32) {
+        const int s = base + lane;
+        const bool in = s < S;
+        const unsigned stopm = __ballot_sync(0xffffffffu, in && sb[s] >= r1);
+        const int lim = stopm ? __ffs(stopm) - 1 : 32;   // lanes at or past the first stop are out
+        const bool valid = in && lane < lim && sb[s + 1] > sb[s];
+        const int val = valid ? ((sa[s] >= 0 && sa[s] < n_ids) ? sa[s] : -1) : 0;
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        if (vm) {
+            const int first = __shfl_sync(0xffffffffu, val, __ffs(vm) - 1);
+            if (!have) {
+                a = first;
+                have = true;
+            }
+            if (__any_sync(0xffffffffu, valid && val != a)) uniform = false;
+        }
+        if (stopm || !uniform) break;
+    }
+    return (have && uniform) ? a : -1;
+}
+
 // Checks a device segment table; every thread of the block calls it (the
 // starts are read in parallel, then OR-reduced).  Sets LORA_DEV_BAD_SEGMENTS.
 __device__ __forceinline__ void check_segments(const int *seg_starts, int S, int T, int *status) {
@@ -225,14 +265,16 @@ bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S, int T, bool units);
 size_t sgmv_plan_bytes(const lora_pool *pool, int matrix, int T);
 // The plan's per-M-tile array (after its items).
 int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan);
-// tile_ad != nullptr (filled by launch_sgmv_tiles): also the fused rows' masks and the units.
+// units: a layer plan -- the plan also classifies the GEMM M-tiles (uniform_tile_adapter, as
+// the tensor-core shrink does), masks the fused rows and lists the shrink and expand units.
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                     int *plan, cudaStream_t st, const int *tile_ad = nullptr);
-// The fused M-tiles' adapters (see sgmv_tile_kernel) into tile_ad, the plan's per-M-tile array;
-// launch_sgmv_plan with that array must follow it in stream order.
-int launch_sgmv_tiles(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                      int *tile_ad, cudaStream_t st);
-int num_sms();   // SMs of the current device (cached)
+                     int *plan, cudaStream_t st, bool units = false);
+int num_sms();   // SMs of the current device (cached per device)
+// Opts kernel `func` in to `bytes` of dynamic shared memory on the current
+// device (raising the attribute only when a launch needs more than before,
+// once per device and kernel; thread safe).  occupancy (optional): resident
+// CTAs per SM of `threads` threads at that size.  LORA_OK or LORA_ERR_CUDA.
+int smem_optin(const void *func, size_t bytes, int threads = 0, int *occupancy = nullptr);
 bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
 // tile_ad != nullptr: M-tiles with tile_ad[m] >= 0 also get that adapter's term
 // s * v . B (v: T x ld_v fp32) inside the GEMM.
@@ -252,7 +294,7 @@ constexpr int kShrinkTcMinRows = 64;
 constexpr int kShrinkTcSegMinRank = 65;
 constexpr int kShrinkTcMaxS = 8192;
 bool shrink_tc_ok(const lora_pool *pool, int h_in, int S);
-int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, const int *tile_ad,
+int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, int *tile_ad,
                      const int *seg_starts, const int *seg_adapter, int S, float *v, int ld_v, cudaStream_t st);
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
                        const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st);

@@ -459,9 +459,10 @@ constexpr uint32_t SK_TMEM_COLS = kFuseMaxRank;
 struct ShrinkTcParams {
     int T, num_k, nsplit;
     int stages, stage_bytes;   // ring depth; bytes of one stage (x tile + npad_max A rows)
-    const int *tile_ad;        // fused layer: per M-tile adapter (or -1); else nullptr
-    const int *seg_starts, *seg_adapter;   // segment tables: tiles of segments with >= min_rows rows
-    int S, min_rows;
+    int *tile_ad;              // fused layer: per M-tile adapter, written here (-1: tile not fused); else nullptr
+    const int *seg_starts, *seg_adapter;   // the batch's segment table
+    int S, min_rows;           // segment tables: tiles of segments with >= min_rows rows
+    int n_ids;                 // fused layer: adapter ids below this may be loaded on the matrix
     PoolView pv;
     int m;
     float *v;
@@ -534,6 +535,37 @@ __device__ __forceinline__ bool wait_cluster_sk(uint64_t *bar, uint32_t parity, 
     }
 }
 
+// Fused layer: the adapter whose term M-tile `mb` gets inside the GEMM (its
+// rows all use that adapter, of rank 1..kFuseMaxRank), or -1.  All threads
+// call it; the segment table is staged in `stage` (2 S + 1 ints of shared
+// memory), then warp 0 decides with uniform_tile_adapter -- the function the
+// rows and plan kernels apply to every tile -- and the first CTA of the cluster
+// publishes the result in tile_ad for the GEMM and the expand that follow.
+__device__ int layer_tile_sk(const ShrinkTcParams &p, int mb, int split, int *stage, SkCtrl *ctrl) {
+    int *sb = stage, *sa = stage + p.S + 1;
+    for (int s = threadIdx.x; s <= p.S; s += kThreadsTC) sb[s] = min(max(p.seg_starts[s], 0), p.T);
+    for (int s = threadIdx.x; s < p.S; s += kThreadsTC) sa[s] = p.seg_adapter[s];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int r0 = mb * BM, r1 = min(p.T, r0 + BM);
+        int a = uniform_tile_adapter(sb, sa, p.S, p.n_ids, r0, r1);
+        if (threadIdx.x == 0) {
+            if (a >= 0) {
+                const int r = a < p.pv.max_adapters
+                                  ? p.pv.table[((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints]
+                                  : -1;
+                if (r < 1 || r > kFuseMaxRank || r > p.ld_v) a = -1;
+            }
+            if (split == 0) p.tile_ad[mb] = a;
+            ctrl->tile[0] = a;
+        }
+    }
+    __syncthreads();
+    const int a = ctrl->tile[0];
+    __syncthreads();    // the staged table (aliasing the ring) is no longer read
+    return a;
+}
+
 // Segment tables: tile `t` among the 128-row pieces of the segments with at
 // least min_rows rows.  All threads call it; ctrl->tile gets the result.
 __device__ void segment_tile_sk(const ShrinkTcParams &p, int t, int *scan, SkCtrl *ctrl) {
@@ -604,7 +636,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (p.tile_ad) {
         row0 = blockIdx.x * BM;
         rows = min(BM, p.T - row0);
-        a = rows > 0 ? p.tile_ad[blockIdx.x] : -1;
+        a = layer_tile_sk(p, blockIdx.x, split, reinterpret_cast<int *>(smem), ctrl);
     } else {
         segment_tile_sk(p, blockIdx.x, reinterpret_cast<int *>(smem), ctrl);
         a = ctrl->tile[0];
@@ -844,13 +876,7 @@ bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t oute
 template <int ST, bool FUSE>
 int launch_gemm_variant(const CUtensorMap &tmx, const CUtensorMap &tmw, const LayerTcParams &p, cudaStream_t st) {
     const size_t smem = (size_t)ST * STAGE_BYTES + (FUSE ? 2 * A2_BYTES + B2_BYTES : 0) + sizeof(Ctrl<ST>) + 1024;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(layer_gemm_tc_kernel<ST, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = true;
-    }
+    if (smem_optin(reinterpret_cast<const void *>(layer_gemm_tc_kernel<ST, FUSE>), smem)) return LORA_ERR_CUDA;
     const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
     layer_gemm_tc_kernel<ST, FUSE><<<grid, kThreadsTC, smem, st>>>(tmx, tmw, p);
     count_launch();
@@ -893,7 +919,7 @@ bool shrink_tc_ok(const lora_pool *pool, int h_in, int S) {
            num_sms() > 0;
 }
 
-int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, const int *tile_ad,
+int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, int *tile_ad,
                      const int *seg_starts, const int *seg_adapter, int S, float *v, int ld_v, cudaStream_t st) {
     CUtensorMap tmx;
     if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM)) return LORA_ERR_CUDA;
@@ -909,6 +935,7 @@ int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x,
     p.seg_adapter = seg_adapter;
     p.S = S;
     p.min_rows = kShrinkTcMinRows;
+    p.n_ids = pool->mat_n_ids[matrix];
     p.pv = pool->view();
     p.m = matrix;
     p.v = v;
@@ -921,7 +948,7 @@ int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x,
     p.stage_bytes = SK_X_BYTES + npad_max * BK * 2;
     const size_t fixed = sizeof(SkCtrl) + 1024;
     const size_t need_recv = (size_t)p.nsplit * BM * ((((npad_max + p.nsplit - 1) / p.nsplit + 3) & ~3) + 4) * 4;
-    const size_t need_scan = tile_ad ? 0 : (size_t)(S + 1) * 4;
+    const size_t need_scan = (size_t)(tile_ad ? 2 * S + 1 : S + 1) * 4;
     p.stages = 0;
     for (size_t budget : {(size_t)113 * 1024, (size_t)227 * 1024}) {
         const int st_n = (int)std::min<size_t>(SK_MAX_STAGES, (budget - fixed) / p.stage_bytes);
@@ -932,13 +959,7 @@ int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x,
     }
     if (p.stages == 0) return LORA_ERR_ARG;       // not reached for ranks <= kFuseMaxRank
     const size_t smem = (size_t)p.stages * p.stage_bytes + fixed;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(shrink_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = smem;
-    }
+    if (smem_optin(reinterpret_cast<const void *>(shrink_tc_kernel), smem)) return LORA_ERR_CUDA;
     const int tiles = tile_ad ? (T + BM - 1) / BM : T / kShrinkTcMinRows;
     if (tiles == 0) return LORA_OK;
     cudaLaunchConfig_t cfg = {};

@@ -6,20 +6,90 @@
 // Serving", question ladder L5): one device array of equal pages and a free
 // list, so adapters of any rank take exactly the pages they need.
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "internal.cuh"
 
 namespace lora {
 
+namespace {
+// Per-device launch facts, looked up under one mutex: SM counts, and for each
+// (device, kernel) the dynamic shared memory it has been opted in to and the
+// resident CTAs per SM measured at given sizes.
+struct FuncEntry {
+    int device;
+    const void *func;
+    size_t optin;           // bytes the attribute was last raised to on this device
+};
+struct OccEntry {
+    int device;
+    const void *func;
+    size_t bytes;
+    int threads;
+    int occ;
+};
+std::mutex g_launch_mu;
+std::vector<FuncEntry> g_funcs;
+std::vector<OccEntry> g_occ;
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {};
+}  // namespace
+
 int num_sms() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
     }
-    return n;
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+int smem_optin(const void *func, size_t bytes, int threads, int *occupancy) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    FuncEntry *fe = nullptr;
+    for (FuncEntry &e : g_funcs)
+        if (e.device == dev && e.func == func) fe = &e;
+    if (!fe) {
+        g_funcs.push_back(FuncEntry{dev, func, 0});
+        fe = &g_funcs.back();
+    }
+    if (bytes > fe->optin) {
+        if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return LORA_ERR_CUDA;
+        }
+        fe->optin = bytes;
+    }
+    if (occupancy) {
+        for (const OccEntry &e : g_occ)
+            if (e.device == dev && e.func == func && e.bytes == bytes && e.threads == threads) {
+                *occupancy = e.occ;
+                return LORA_OK;
+            }
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, func, threads, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return LORA_ERR_CUDA;
+        }
+        g_occ.push_back(OccEntry{dev, func, bytes, threads, occ});
+        *occupancy = occ;
+    }
+    return LORA_OK;
 }
 
 std::atomic<unsigned long long> g_launches{0};
@@ -103,42 +173,45 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
     const bool tc = gemm_tc_ok(p, h_in, h_out, T);
     const bool tcs = tc && shrink_tc_ok(p, h_in, S);
     if (sgmv_plan_ok(p, matrix, S, T, tcs) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
-        // 1. GEMM M-tiles whose rows share one adapter (tensor-core tiles)
-        // 2. (tensor cores) v of those tiles: M 128 x N r contractions, K split over a cluster
-        // 3. plan: the other rows' tokens grouped by adapter, as cost-ordered work units
-        // 4. v of every other adapted token (warp-MMA SGMV shrink)
-        // 5. base product; the uniform tiles add their low-rank term inside the GEMM
-        // 6. expand the remaining rows
-        // With tensor-core tiles, 3 and 4 read only the segment table, the tile flags and x
-        // and write only the plan and v rows outside those tiles, which 2 and 5 never touch:
-        // they run on a side stream beside them and join before 6.  Without, the plan
-        // comes first on the one stream.
+        // With tensor-core tiles (tcs):
+        //   main stream: (1) the tensor-core shrink, whose CTAs also decide which
+        //     128-row GEMM M-tiles have one adapter for all their rows (tile_ad),
+        //     computes v of those tiles; (2) the GEMM adds their low-rank term
+        //     itself; after the join, (3) the expand of the remaining rows.
+        //   side stream, forked at the start: the plan (the other rows' tokens
+        //     grouped by adapter as cost-ordered work units; it classifies the
+        //     M-tiles itself with the same function) and the warp-MMA shrink of
+        //     those rows.  They read only the segment table, the pool's ranks
+        //     and x, and write only the plan and v rows outside fused tiles,
+        //     which (1) and (2) never touch.
+        // Without tensor-core tiles everything runs on the one stream: plan,
+        // shrink, base product, expand.
         int *plan = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(v + (size_t)T * p->max_rank) + 255) &
                                             ~uintptr_t(255));
-        int *tile_ad = tcs ? sgmv_plan_tiles(p, matrix, T, plan) : nullptr;
-        rc = tcs ? launch_sgmv_tiles(p, matrix, seg_starts, seg_adapter, S, T, tile_ad, st)
-                 : launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st, nullptr);
-        if (rc) return rc;
-        SideStream *side = tcs ? side_stream() : nullptr;
-        if (side && cudaEventRecord(side->fork, st) != cudaSuccess) return LORA_ERR_CUDA;
-        if (tcs && (rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, nullptr, nullptr, 0, v, p->max_rank, st)))
-            return rc;
+        if (!tcs) {
+            if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st))) return rc;
+            if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st)))
+                return rc;
+            rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st) : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+            if (rc) return rc;
+            return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st);
+        }
+        int *tile_ad = sgmv_plan_tiles(p, matrix, T, plan);
+        SideStream *side = side_stream();
         cudaStream_t st3 = st;
+        if (side && cudaEventRecord(side->fork, st) != cudaSuccess) return LORA_ERR_CUDA;
+        // the tensor-core shrink is enqueued first, so its CTAs take the SMs first
+        rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, seg_starts, seg_adapter, S, v, p->max_rank, st);
         if (side) {
             if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return LORA_ERR_CUDA;
             st3 = side->s;
         }
-        rc = tcs ? launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st3, tile_ad) : LORA_OK;
+        if (!rc) rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st3, true);
         if (!rc)
-            rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st3,
-                                    tcs);
+            rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st3, true);
         if (side && cudaEventRecord(side->join, side->s) != cudaSuccess) return LORA_ERR_CUDA;
-        if (rc) {
-            if (side) cudaStreamWaitEvent(st, side->join, 0);     // no side work is left unjoined
-            return rc;
-        }
-        rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank)
-                : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+        if (!rc) rc = launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank);
+        // no side work is left unjoined, error or not
         if (side && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return LORA_ERR_CUDA;
         if (rc) return rc;
         return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st,

@@ -270,62 +270,15 @@ struct PlanParams {
     int max_items;
     PoolView pv;        // for ranks of the tile classification
     int m;
-    const int *tile_ad; // nullptr, or [n_tiles] from sgmv_tile_kernel: the fused M-tiles' adapters, -1 if none
+    bool units;         // layer plan: classify the GEMM M-tiles (as the tensor-core shrink does) and list units
     int n_tiles;
-    Unit *su, *eu;      // with tile_ad: shrink and expand units of the work items (counts plan[2], plan[3])
+    Unit *su, *eu;      // with units: shrink and expand units of the work items (counts plan[2], plan[3])
     int npc_s;          // ranks per shrink unit
     int nb_total;       // column blocks of kNb in h_out
     int bpu;            // column blocks per expand unit of cheap items
     int rank_cap;       // ranks beyond this are not computed (the v row length)
     int body;           // ints of the counting-sort area of shared memory
 };
-
-// GEMM M-tiles whose rows all use one adapter of rank 1..kFuseMaxRank: the
-// GEMM adds that adapter's term itself (and the tensor-core shrink computes
-// its v), so the plan leaves those rows out of its units.  One CTA: the
-// segment table in shared memory, a thread per tile.
-struct TileParams {
-    const int *seg_starts, *seg_adapter;
-    int S, T;
-    int n_ids;          // adapter ids below this may be loaded on the matrix
-    PoolView pv;
-    int m;
-    int *tile_ad;       // output [n_tiles]: the tile's adapter, -1 if the tile is not fused
-    int n_tiles;
-};
-
-__global__ void __launch_bounds__(kPlanThreads) sgmv_tile_kernel(TileParams p) {
-    extern __shared__ __align__(16) int sm[];
-    int *sb = sm;                        // [S + 1] segment bounds, clamped into [0, T]
-    int *sa = sb + p.S + 1;              // [S] segment adapters (-1: none or invalid)
-    for (int s = threadIdx.x; s <= p.S; s += kPlanThreads) sb[s] = min(max(p.seg_starts[s], 0), p.T);
-    for (int s = threadIdx.x; s < p.S; s += kPlanThreads) {
-        const int a = p.seg_adapter[s];
-        sa[s] = a < p.n_ids ? a : -1;
-    }
-    __syncthreads();
-    for (int mb = threadIdx.x; mb < p.n_tiles; mb += kPlanThreads) {
-        const int r0 = mb * kTileRows, r1 = min(p.T, r0 + kTileRows);
-        int lo = 0, hi = p.S;                   // first segment bound above r0
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sb[mid] > r0) hi = mid; else lo = mid + 1;
-        }
-        int a = -2;
-        bool uniform = true;
-        for (int s = max(lo - 1, 0); s < p.S && sb[s] < r1 && uniform; ++s) {
-            if (sb[s + 1] <= sb[s]) continue;
-            if (a == -2) a = sa[s];
-            else if (sa[s] != a) uniform = false;
-        }
-        int out = -1;
-        if (uniform && a >= 0 && a < p.n_ids) {
-            const int rank = p.pv.table[((long long)a * p.pv.n_matrices + p.m) * p.pv.rec_ints];
-            if (rank >= 1 && rank <= kFuseMaxRank) out = a;
-        }
-        p.tile_ad[mb] = out;
-    }
-}
 
 // Column blocks per expand unit from an item's cost per block: its y rows,
 // read and written once per pass of up to 32 ranks, plus its B rows.
@@ -342,8 +295,9 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     int *segoff = ibase + p.n_ids;       // [S] offset of each segment within its adapter's tokens
     int *sb = segoff + p.S;              // [S + 1] segment bounds, clamped into [0, T]
     int *sa = sb + p.S + 1;              // [S] segment adapters (-1: none or invalid)
-    int *arank = sa + p.S;               // with tile_ad: [n_ids] each adapter's rank on the matrix
-    int *sperm = arank + p.n_ids;        // with tile_ad: [T] copy of the token permutation
+    int *arank = sa + p.S;               // with units: [n_ids] each adapter's rank on the matrix
+    int *sperm = arank + p.n_ids;        // with units: [T] copy of the token permutation
+    int *tflag = sperm + p.T;            // with units: [n_tiles] the adapter of each GEMM-fused M-tile, or -1
     int *wtot = sm + p.body;             // [kPlanThreads / 32 + 1], then the work count
     // with units: [max_items] int4 work items, int4 unit counts and ranks, after the counters
     int4 *sitem = reinterpret_cast<int4 *>(sm + p.body + ((kPlanThreads / 32 + 2 + 3) & ~3));
@@ -353,11 +307,11 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int nwarps = kPlanThreads / 32;
     // one round of global loads: segment bounds (checked as they arrive), segment
-    // adapters and, with tile_ad, every adapter's rank
+    // adapters and, with units, every adapter's rank
     bool bad = false;
     for (int i = tid; i < p.n_ids; i += kPlanThreads) {
         cnt[i] = 0;
-        if (p.tile_ad) arank[i] = p.pv.table[((long long)i * p.pv.n_matrices + p.m) * p.pv.rec_ints];
+        if (p.units) arank[i] = p.pv.table[((long long)i * p.pv.n_matrices + p.m) * p.pv.rec_ints];
     }
     for (int s = tid; s <= p.S; s += kPlanThreads) {
         const int b0 = p.seg_starts[s];
@@ -412,7 +366,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         for (int i = 0; i < n; ++i)
             if (dst + i < p.T) {
                 perm[dst + i] = sb[s] + i;
-                if (p.tile_ad) sperm[dst + i] = sb[s] + i;
+                if (p.units) sperm[dst + i] = sb[s] + i;
             }
     }
     for (int s = warp; s < p.S; s += nwarps) {
@@ -422,19 +376,21 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
         for (int i = lane; i < n; i += 32)
             if (dst + i < p.T) {
                 perm[dst + i] = sb[s] + i;
-                if (p.tile_ad) sperm[dst + i] = sb[s] + i;
+                if (p.units) sperm[dst + i] = sb[s] + i;
             }
     }
-    if (!p.tile_ad) return;
+    if (!p.units) return;
     int *wcount = wtot + nwarps + 1;        // past block_scan's words
     if (tid == 0) *wcount = 0;
-    // the GEMM-fused M-tiles (sgmv_tile_kernel's flags), kept in shared memory
-    // (in the counters' space, free by now) when they fit there
-    __syncthreads();
-    int *tflag = cnt;
-    const bool staged = p.n_tiles <= 3 * p.n_ids + p.S;
-    if (staged)
-        for (int mb = tid; mb < p.n_tiles; mb += kPlanThreads) tflag[mb] = p.tile_ad[mb];
+    // the GEMM-fused M-tiles, decided as the tensor-core shrink decides them
+    // (same function, same table; a warp per tile): the adapter of a tile
+    // whose rows all use it, when its rank is 1..kFuseMaxRank
+    for (int mb = warp; mb < p.n_tiles; mb += nwarps) {
+        const int r0 = mb * kTileRows, r1 = min(p.T, r0 + kTileRows);
+        const int a = uniform_tile_adapter(sb, sa, p.S, p.n_ids, r0, r1);
+        if (lane == 0)
+            tflag[mb] = (a >= 0 && arank[a] >= 1 && arank[a] <= kFuseMaxRank && arank[a] <= p.rank_cap) ? a : -1;
+    }
     __syncthreads();
     // each item's mask of rows that sit in such tiles (the expand skips them;
     // the item's perm entries are read with independent loads); items that keep
@@ -455,7 +411,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
                 unsigned mask = 0;
 #pragma unroll
                 for (int k = 0; k < kM; ++k)
-                    if (tk[k] >= 0 && tk[k] < p.T && (staged ? tflag[tk[k] / kTileRows] : p.tile_ad[tk[k] / kTileRows]) >= 0)
+                    if (tk[k] >= 0 && tk[k] < p.T && tflag[tk[k] / kTileRows] >= 0)
                         mask |= 1u << k;
                 const unsigned all = it.nt >= 32 ? 0xffffffffu : ((1u << it.nt) - 1u);
                 want = (mask & all) != all;        // rows left for the SGMV kernels (slot order is immaterial)
@@ -1013,6 +969,111 @@ __device__ __forceinline__ void expand_unit(const ExpandParams &p, const Item &i
     const int mg = warp & 1, nh = warp >> 1;
     const int g = lane >> 2, q = lane & 3;
 
+    const int passes = (r + kpc - 1) / kpc;
+    if (nb == 1 && passes > 1 && passes <= kStagesE && 2 * vp <= yp) {
+        // One column block and several rank passes (the costly units of high-rank
+        // adapters): y is read and written once, the B chunks of every pass are
+        // copied at once into the ring's B slots (pass j -> stage j), the scaled v
+        // of pass 0 goes to svh/svl and that of pass j >= 1 to stage j's unused y
+        // slot (both parts fit there: 2 vp <= yp), and the passes' products
+        // accumulate in registers before the one rounding of y.
+        const int n0 = b_first * kNb;
+        const int ncv = min(kNb, p.h_out - n0) / 8;
+        for (int i = tid; i < nt * 16; i += kThreadsE) {
+            const int row = i >> 4, cv = i & 15;
+            if (cv < ncv) cp_async16(sy + row * yp + cv * 8, p.y + (long long)tok[row] * p.h_out + n0 + cv * 8);
+        }
+        for (int j = 0; j < passes; ++j) {
+            const int jj0 = j * kpc, rn = min(kpc, r - jj0), kpad = (rn + 15) & ~15;
+            __nv_bfloat16 *db = sb + j * kpc * yp;
+            for (int i = tid; i < kpad * 16; i += kThreadsE) {
+                const int row = i >> 4, cv = i & 15;
+                if (row < rn) {
+                    if (cv < ncv)
+                        cp_async16(db + row * yp + cv * 8,
+                                   page_row<__nv_bfloat16>(p.pv, clamp_page(p.pv, rec[kRecHeader + r_rec + jj0 + row])) +
+                                       n0 + cv * 8);
+                } else {
+                    *reinterpret_cast<uint4 *>(db + row * yp + cv * 8) = make_uint4(0, 0, 0, 0);   // MMA K padding
+                }
+            }
+        }
+        cp_commit();
+        const bool vec = (p.ld_v & 3) == 0;
+        for (int j = 0; j < passes; ++j) {
+            const int jj0 = j * kpc, rn = min(kpc, r - jj0), kpad = (rn + 15) & ~15;
+            __nv_bfloat16 *vh = j == 0 ? svh : sy + j * kM * yp;
+            __nv_bfloat16 *vl = j == 0 ? svl : vh + kM * vp;
+            for (int i = tid; i < kM * (kpad >> 2); i += kThreadsE) {
+                const int row = i / (kpad >> 2), jl = 4 * (i % (kpad >> 2));
+                float e4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (row < nt && jl < rn) {
+                    const float *src = p.v + (long long)tok[row] * p.ld_v + jj0 + jl;
+                    if (vec) {       // ld_v % 4 == 0 and jj0 % 4 == 0: the group stays in the row
+                        const float4 f = *reinterpret_cast<const float4 *>(src);
+                        e4[0] = f.x; e4[1] = f.y; e4[2] = f.z; e4[3] = f.w;
+                    } else {
+                        for (int e = 0; e < 4; ++e)
+                            if (jl + e < rn) e4[e] = src[e];
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float val = jl + e < rn ? scale * e4[e] : 0.f;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+                    vh[row * vp + jl + e] = hi;
+                    vl[row * vp + jl + e] = __float2bfloat16_rn(val - __bfloat162float(hi));
+                }
+            }
+        }
+        cp_wait<0>();
+        __syncthreads();
+        float d[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+        for (int j = 0; j < passes; ++j) {
+            const int rn = min(kpc, r - j * kpc), kpad = (rn + 15) & ~15;
+            const __nv_bfloat16 *vh = j == 0 ? svh : sy + j * kM * yp;
+            const __nv_bfloat16 *vl = j == 0 ? svl : vh + kM * vp;
+            const __nv_bfloat16 *tb = sb + j * kpc * yp;
+            for (int kk = 0; kk < kpad; kk += 16) {
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                ldsm_x4(vh + (mg * 16 + (lane & 15)) * vp + kk + (lane >> 4) * 8, h0, h1, h2, h3);
+                ldsm_x4(vl + (mg * 16 + (lane & 15)) * vp + kk + (lane >> 4) * 8, l0, l1, l2, l3);
+#pragma unroll
+                for (int t = 0; t < 8; t += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(tb + (kk + (lane & 7) + ((lane >> 3) & 1) * 8) * yp + nh * 64 + (t + (lane >> 4)) * 8,
+                              b0, b1, b2, b3);
+                    mma16816(d[t], h0, h1, h2, h3, b0, b1);
+                    mma16816(d[t], l0, l1, l2, l3, b0, b1);
+                    mma16816(d[t + 1], h0, h1, h2, h3, b2, b3);
+                    mma16816(d[t + 1], l0, l1, l2, l3, b2, b3);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = mg * 16 + g + 8 * h;
+                __nv_bfloat162 *yy = reinterpret_cast<__nv_bfloat162 *>(sy + row * yp + nh * 64 + t * 8 + 2 * q);
+                const float2 f = __bfloat1622float2(*yy);
+                *yy = __floats2bfloat162_rn(f.x + d[t][2 * h], f.y + d[t][2 * h + 1]);
+            }
+        __syncthreads();
+        for (int i = tid; i < nt * (kNb / 8); i += kThreadsE) {
+            const int row = i >> 4, cv = i & 15;
+            if (cv < ncv)
+                *reinterpret_cast<uint4 *>(p.y + (long long)tok[row] * p.h_out + n0 + cv * 8) =
+                    *reinterpret_cast<const uint4 *>(sy + row * yp + cv * 8);
+        }
+        __syncthreads();   // shared memory is read before the next unit reuses it
+        return;
+    }
+
     // ranks in passes of kpc; each pass streams the unit's y blocks once
     for (int j0 = 0; j0 < r; j0 += kpc) {
         const int rn = min(kpc, r - j0);
@@ -1236,7 +1297,8 @@ int *sgmv_plan_tiles(const lora_pool *pool, int matrix, int T, int *plan) {
 // for layer plans, the unit-building arrays.
 static size_t plan_smem(const lora_pool *pool, int matrix, int S, int T, bool units, int *body) {
     const int n_ids = pool->mat_n_ids[matrix];
-    *body = (3 * n_ids + 3 * S + 1 + (units ? n_ids + T : 0) + 3) & ~3;
+    const int n_tiles = (T + kTileRows - 1) / kTileRows;
+    *body = (3 * n_ids + 3 * S + 1 + (units ? n_ids + T + n_tiles : 0) + 3) & ~3;
     size_t ints = (size_t)*body + ((kPlanThreads / 32 + 2 + 3) & ~3);
     if (units) ints += (size_t)9 * plan_layout(pool, matrix, T).max_items + 4 * (kPlanThreads / 32 + 1);
     return ints * 4;
@@ -1247,33 +1309,8 @@ bool sgmv_plan_ok(const lora_pool *pool, int matrix, int S, int T, bool units) {
     return pool->mat_n_ids[matrix] > 0 && S <= kMaxS && plan_smem(pool, matrix, S, T, units, &body) <= 160 * 1024;
 }
 
-int launch_sgmv_tiles(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                      int *tile_ad, cudaStream_t st) {
-    TileParams p;
-    p.seg_starts = seg_starts;
-    p.seg_adapter = seg_adapter;
-    p.S = S;
-    p.T = T;
-    p.n_ids = pool->mat_n_ids[matrix];
-    p.pv = pool->view();
-    p.m = matrix;
-    p.tile_ad = tile_ad;
-    p.n_tiles = (T + kTileRows - 1) / kTileRows;
-    const size_t smem = (size_t)(2 * S + 1) * 4;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(sgmv_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = smem;
-    }
-    sgmv_tile_kernel<<<1, kPlanThreads, smem, st>>>(p);
-    count_launch();
-    return cuda_status(cudaGetLastError());
-}
-
 int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, const int *seg_adapter, int S, int T,
-                     int *plan, cudaStream_t st, const int *tile_ad) {
+                     int *plan, cudaStream_t st, bool units) {
     const PlanLayout L = plan_layout(pool, matrix, T);
     PlanParams p;
     p.seg_starts = seg_starts;
@@ -1286,22 +1323,16 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.max_items = L.max_items;
     p.pv = pool->view();
     p.m = matrix;
-    p.tile_ad = tile_ad;
+    p.units = units;
     p.n_tiles = (T + kTileRows - 1) / kTileRows;
-    p.su = tile_ad ? reinterpret_cast<Unit *>(plan + L.su) : nullptr;
-    p.eu = tile_ad ? reinterpret_cast<Unit *>(plan + L.eu) : nullptr;
+    p.su = units ? reinterpret_cast<Unit *>(plan + L.su) : nullptr;
+    p.eu = units ? reinterpret_cast<Unit *>(plan + L.eu) : nullptr;
     p.npc_s = shrink_npc(pool);
     p.nb_total = (std::max(0, pool->mat_h_out[matrix]) + kNb - 1) / kNb;
     p.bpu = 8;
     p.rank_cap = pool->max_rank;
-    const size_t smem = plan_smem(pool, matrix, S, T, tile_ad != nullptr, &p.body);
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(sgmv_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = smem;
-    }
+    const size_t smem = plan_smem(pool, matrix, S, T, units, &p.body);
+    if (smem_optin(reinterpret_cast<const void *>(sgmv_plan_kernel), smem)) return LORA_ERR_CUDA;
     sgmv_plan_kernel<<<1, kPlanThreads, smem, st>>>(p);
     count_launch();
     return cuda_status(cudaGetLastError());
@@ -1327,16 +1358,9 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
         p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).su);
         const size_t smem = (size_t)kStagesS * (kRowsS + p.npc) * (kKs + 8) * 2 + (size_t)4 * 16 * p.npc * 4 +
                             (size_t)(kRowsS + p.pv.rec_ints) * 4 + 16;
-        static size_t configured_u = 0;
-        static int occ = 0;
-        if (smem > configured_u) {
-            if (cudaFuncSetAttribute(sgmv_shrink_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgmv_shrink_units_kernel, kThreadsS, smem) !=
-                    cudaSuccess)
-                return LORA_ERR_CUDA;
-            configured_u = smem;
-        }
+        int occ = 0;
+        if (smem_optin(reinterpret_cast<const void *>(sgmv_shrink_units_kernel), smem, kThreadsS, &occ))
+            return LORA_ERR_CUDA;
         const int nk = h_in / kKs;
         const int ks = nk >= 16 ? 2 : 1;       // measured: 2 beats 1 and 4 (4 leaves too few clusters)
         const int clusters = std::max(1, num_sms() * std::max(1, occ) / ks);
@@ -1366,13 +1390,7 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
                              ~(size_t)15;
         p.alias_bytes = (int)alias;
         const size_t smem_w = alias + (size_t)(kRowsW + kThreadsW / 32 + 4 + p.pv.rec_ints) * 4;
-        static size_t configured_w = 0;
-        if (smem_w > configured_w) {
-            if (cudaFuncSetAttribute(sgmv_shrink_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_w) != cudaSuccess)
-                return LORA_ERR_CUDA;
-            configured_w = smem_w;
-        }
+        if (smem_optin(reinterpret_cast<const void *>(sgmv_shrink_wide_kernel), smem_w)) return LORA_ERR_CUDA;
         const dim3 grid_w(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc, 1);
         sgmv_shrink_wide_kernel<<<grid_w, kThreadsW, smem_w, st>>>(p);
         count_launch();
@@ -1382,13 +1400,7 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
     p.alias_bytes = 0;
     const size_t smem = (size_t)kStagesS * (kRowsS + p.npc) * (kKs + 8) * 2 + (size_t)3 * 16 * p.npc * 4 +
                         (size_t)(kRowsS + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(sgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = smem;
-    }
+    if (smem_optin(reinterpret_cast<const void *>(sgmv_shrink_kernel), smem)) return LORA_ERR_CUDA;
     const dim3 grid(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc, kM / kRowsS);
     sgmv_shrink_kernel<<<grid, kThreadsS, smem, st>>>(p);
     count_launch();
@@ -1414,13 +1426,7 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
     p.ncg = (nb_total + p.bpu - 1) / p.bpu;
     const size_t smem = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
                         (size_t)(kM + 8 + p.pv.rec_ints + (plan ? 0 : S + 1)) * 4 + 16;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(sgmv_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return LORA_ERR_CUDA;
-        configured = smem;
-    }
+    if (smem_optin(reinterpret_cast<const void *>(sgmv_expand_kernel), smem)) return LORA_ERR_CUDA;
     if (tile_ad && plan) {
         // layer plan: persistent CTAs over the plan's expand units, in passes of at most 32
         // ranks (a third CTA per SM; only units of ranks above 32 take more passes)
@@ -1428,16 +1434,9 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
         p.kpc = std::min(32, p.kpc);
         const size_t smem_u = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
                               (size_t)(kM + 8 + p.pv.rec_ints) * 4 + 16;
-        static size_t configured_u = 0;
-        static int occ = 0;
-        if (smem_u > configured_u) {
-            if (cudaFuncSetAttribute(sgmv_expand_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_u) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sgmv_expand_units_kernel, kThreadsE, smem_u) !=
-                    cudaSuccess)
-                return LORA_ERR_CUDA;
-            configured_u = smem_u;
-        }
+        int occ = 0;
+        if (smem_optin(reinterpret_cast<const void *>(sgmv_expand_units_kernel), smem_u, kThreadsE, &occ))
+            return LORA_ERR_CUDA;
         sgmv_expand_units_kernel<<<num_sms() * std::max(1, occ), kThreadsE, smem_u, st>>>(p);
         count_launch();
         return cuda_status(cudaGetLastError());
