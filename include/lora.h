@@ -11,8 +11,8 @@
  * is a gather of small matmuls, "shrink" (x -> v, width r) then "expand"
  * (v -> y).  SGMV serves contiguous segments of tokens that share an adapter
  * (prefill), BGMV one adapter per token (decode).  Adapters of different
- * ranks live in one paged pool ("A page holds H elements ... rank R -> R
- * pages", S-LoRA slide 8) and are gathered without padding to a common rank
+ * ranks live in one paged pool (S-LoRA slide 8: pages of H elements, R of them
+ * for a rank-R adapter) and are gathered without padding to a common rank
  * (S-LoRA slide 10, MBGMM/MBGMV).
  *
  * Orientation used throughout.  For adapter a on one adapted matrix:
@@ -113,10 +113,10 @@ int lora_pool_destroy(lora_pool *pool);
  *   B    rank x h_out (row-major, pool dtype).
  * The first load on a matrix fixes that matrix's (h_in, h_out); later loads
  * must match (else LORA_ERR_SHAPE).  A previous adapter in the same entry is
- * replaced.  The device copy and the table update run on `stream` (after the
- * work already queued there) and the call returns once they are complete:
- * the adapter is resident for every kernel launched afterwards, on any
- * stream, and the host arrays may be freed at once.
+ * replaced (the device is synchronised first).  The device copy and the table
+ * update run on `stream` (after the work already queued there) and the call
+ * returns once they are complete: the adapter is resident for every kernel
+ * launched afterwards, on any stream, and the host arrays may be freed at once.
  * rank == 0 is legal (the adapter adds nothing).
  * Errors: LORA_ERR_ARG, LORA_ERR_RANK, LORA_ERR_SHAPE, LORA_ERR_POOL_FULL
  * (the pool is unchanged), LORA_ERR_CUDA.
@@ -129,7 +129,56 @@ int lora_pool_load(lora_pool *pool, int adapter, int matrix, int rank, float sca
  * Errors: LORA_ERR_ARG, LORA_ERR_NOT_LOADED, LORA_ERR_CUDA. */
 int lora_pool_unload(lora_pool *pool, int adapter, int matrix);
 
-/* Pages currently free (host bookkeeping; no device access). -1 on NULL. */
+/*
+ * Asynchronous upload (S-LoRA slide 9: the adapters that queued requests will
+ * need are copied to the GPU while the current batch computes; "Multi-LoRA
+ * Serving", section "Memory: slots, tiers and paging": a host-memory tier with
+ * prefetch lets one GPU serve far more adapters than its slots hold).
+ *
+ * lora_pool_load_async takes the arguments of lora_pool_load and copies the
+ * host arrays into a pinned staging slot of the pool (a CPU copy: A_T and B
+ * may be freed when the call returns), then ENQUEUES on `stream` the copy to
+ * the device, the scatter into the adapter's pages and the copy of its table
+ * record, and returns without waiting for them.  The adapter is resident for
+ * work enqueued on `stream` after the call, and for work on other streams
+ * ordered after it (an event recorded on `stream` after the call).  Kernels
+ * of this library launched on `stream` right after it read the new record
+ * (the record copy is the last step and is not a kernel).
+ * Replacing an adapter: every kernel that may still read the old one must be
+ * ordered before the call (same stream, or an event); its pages return to the
+ * free list only once `stream` has passed the table update.
+ * The staging ring has a few slots; a call that finds its slot still in use
+ * waits for that slot's earlier copies.  When the free list is short, pages
+ * retired by earlier asynchronous calls are waited for (oldest first).
+ * Errors: as lora_pool_load (the pool is unchanged on any error).
+ */
+int lora_pool_load_async(lora_pool *pool, int adapter, int matrix, int rank, float scale,
+                         int h_in, int h_out, const void *A_T, const void *B, lora_stream stream);
+
+/* Marks the entry unloaded by a copy enqueued on `stream` (no wait); its
+ * pages return to the free list once `stream` has passed it.  Kernels that
+ * may still read the entry must be ordered before the call.
+ * Errors: LORA_ERR_ARG, LORA_ERR_NOT_LOADED, LORA_ERR_CUDA. */
+int lora_pool_unload_async(lora_pool *pool, int adapter, int matrix, lora_stream stream);
+
+/* One adapter of a prefetch list: lora_pool_load's arguments. */
+typedef struct lora_adapter_src {
+    int adapter, matrix, rank;
+    float scale;
+    int h_in, h_out;
+    const void *A_T;   /* rank x h_in, host, pool dtype */
+    const void *B;     /* rank x h_out, host, pool dtype */
+} lora_adapter_src;
+
+/* Prefetch: lora_pool_load_async for every entry of `list` whose (adapter,
+ * matrix) is not resident yet (resident entries are left as they are), in
+ * list order, on `stream`.  Returns the number of uploads enqueued (>= 0), or
+ * the first error (entries before it stay enqueued). */
+int lora_pool_prefetch(lora_pool *pool, const lora_adapter_src *list, int n, lora_stream stream);
+
+/* Pages currently free (host bookkeeping; pages retired by asynchronous calls
+ * count once the stream has passed them -- an event query, no wait). -1 on
+ * NULL. */
 int lora_pool_free_pages(const lora_pool *pool);
 
 /*
@@ -167,8 +216,9 @@ size_t lora_layer_forward_workspace_size(const lora_pool *pool, int matrix, int 
 
 /*
  * Adapted layer: the shared base product for the whole mixed batch plus each
- * token's own low-rank term ("runs the base matmul once, then applies each
- * adapter's low-rank update"):
+ * token's own low-rank term (the base product is computed once for every
+ * token, and each token then receives its own adapter's update, "Multi-LoRA
+ * Serving", section "The kernel trick: gather, do not merge"):
  *   y[t][n] = sum_k x[t][k] * W[n][k] + scale_a * sum_j (sum_k x[t][k] A_T_a[j][k]) B_a[j][n]
  * y is OVERWRITTEN.  W: h_out x h_in (pool dtype).  Tokens without an
  * adapter (or with an invalid one) get the base term only.

@@ -19,10 +19,11 @@
  *     y[t][n] = y0[t][n] + sum_k x[t][k] * W[n][k]             (base, optional)
  *                        + scale_a * sum_j v[t][j] * B_a[j][n]  ("expand")
  *
- * Segments ("SGMV ... contiguous segments of tokens sharing an adapter") are
- * expanded to one adapter id per token by a plain loop.  Mixed ranks ("Kernels
- * gather mixed-rank adapters without padding", S-LoRA slide 10) are handled by
- * giving each adapter its own rank: the sums over j run to that rank only.
+ * Segments (SGMV: runs of consecutive tokens that share an adapter) are
+ * expanded to one adapter id per token by a plain loop.  Mixed ranks (S-LoRA
+ * slide 10: adapters of different ranks are gathered without padding them to
+ * one rank) are handled by giving each adapter its own rank: the sums over j
+ * run to that rank only.
  *
  * Conventions the pages leave open, taken here:
  *   - adapter id < 0 means "no adapter": the token gets no low-rank term;

@@ -1,5 +1,5 @@
-// BGMV for decode batches: "batched gather matrix-vector, one adapter per
-// decode token" ("Multi-LoRA Serving", section "The kernel trick: gather, do
+// BGMV for decode batches: every decode token gathers the low-rank factors of
+// its own adapter ("Multi-LoRA Serving", section "The kernel trick: gather, do
 // not merge"), with per-adapter ranks as in S-LoRA's MBGMV (slide 10).
 //
 //   y[t][n] += s_a * sum_j (sum_k x[t][k] * A_T_a[j][k]) * B_a[j][n],  a = token_adapter[t]

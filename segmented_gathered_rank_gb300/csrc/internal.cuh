@@ -4,8 +4,8 @@
 //   pages   n_pages x page_elems elements of the pool dtype.  One page holds
 //           one row of A_T (h_in elements) or one row of B (h_out elements);
 //           a rank-r adapter on one matrix owns 2r pages anywhere in the
-//           pool ("A page holds H elements ... rank R -> R pages", S-LoRA
-//           slide 8), so mixed ranks need no padding.
+//           pool (S-LoRA slide 8: pages of H elements, R of them for a
+//           rank-R adapter), so mixed ranks need no padding.
 //   table   one record of rec_ints int32 per (adapter, matrix), record index
 //           adapter * n_matrices + matrix:
 //             [0] rank (-1 = not loaded)   [1] scale (float bits)
@@ -74,11 +74,24 @@ struct lora_pool {
     std::vector<int> mat_h_out;
     std::vector<int> mat_n_ids;       // per matrix: 1 + largest adapter id ever loaded
     std::vector<int> mat_max_rank;    // per matrix: largest rank ever loaded
-    // load staging: pinned host buffer -> device buffer -> scatter kernel
-    void *h_stage;
-    void *d_stage;
+    // load staging: a ring of n_slots slots, each a pinned host buffer -> a device
+    // buffer -> the scatter kernel and the record copy; a slot is reused once the
+    // event recorded after its last copy has completed
+    void *h_stage;                    // n_slots x stage_bytes, pinned
+    void *d_stage;                    // n_slots x stage_bytes
     size_t stage_bytes;
-    cudaEvent_t stage_done;
+    int n_slots;
+    int next_slot;
+    std::vector<cudaEvent_t> slot_done;
+    std::vector<char> slot_busy;
+    // pages of replaced or unloaded adapters: back to the free list once the
+    // event recorded after the table update that retired them has completed
+    struct Deferred {
+        std::vector<int> pages;
+        cudaEvent_t done;
+    };
+    std::vector<Deferred> deferred;
+    std::vector<cudaEvent_t> spare_events;
 
     lora::PoolView view() const {
         lora::PoolView v;

@@ -1,9 +1,8 @@
 // CUDA-core kernels for the gathered low-rank update: one thread block per
-// token.  BGMV ("batched gather matrix-vector, one adapter per decode
-// token") fuses shrink and expand; SGMV ("segmented gather, for contiguous
-// segments of tokens sharing an adapter") runs them as two launches with v
-// in between ("Multi-LoRA Serving", section "The kernel trick: gather, do
-// not merge").  Ranks are per adapter (S-LoRA slide 10, MBGMM/MBGMV): the
+// token.  BGMV (each decode token gathers its own adapter) fuses shrink and
+// expand; SGMV (runs of consecutive tokens share an adapter) runs them as two
+// launches with v in between ("Multi-LoRA Serving", section "The kernel trick:
+// gather, do not merge").  Ranks are per adapter (S-LoRA slide 10, MBGMM/MBGMV): the
 // loops over j run to the adapter's own rank.
 #include "internal.cuh"
 

@@ -1,10 +1,11 @@
 // Paged adapter pool and the C-ABI entry points.
 //
-// The pool follows S-LoRA's unified paging ("A page holds H elements ...
-// rank R -> R pages", slide 8; "Adapters of different ranks ... would
-// fragment memory; one paged pool keeps utilisation high", "Multi-LoRA
-// Serving", question ladder L5): one device array of equal pages and a free
+// The pool follows S-LoRA's unified paging (slide 8: memory is cut into pages
+// of H elements and a rank-R adapter takes R of them; "Multi-LoRA Serving",
+// question ladder: mixed ranks in fixed-size slots would fragment memory,
+// one paged pool avoids that): one device array of equal pages and a free
 // list, so adapters of any rank take exactly the pages they need.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -94,9 +95,11 @@ int smem_optin(const void *func, size_t bytes, int threads, int *occupancy) {
 
 std::atomic<unsigned long long> g_launches{0};
 
-// Copies one staged row per block into its page and (block 0) writes the
-// record.  Staged layout: rows of A_T then rows of B, each `row_bytes[...]`
-// long, packed back to back at 16-byte multiples.
+// Copies one staged row per block into its page.  Staged layout: rows of A_T
+// then rows of B, each `row_bytes[...]` long, packed back to back at 16-byte
+// multiples.  The record that points at the pages is copied after this kernel
+// (a plain host-to-device copy, see enqueue_load), so a kernel that reads it
+// finds the pages written.
 struct LoadArgs {
     int rec_index;
     int rank;
@@ -107,8 +110,7 @@ struct LoadArgs {
 };
 
 __global__ void load_scatter_kernel(const uint8_t *__restrict__ stage, uint8_t *__restrict__ pages,
-                                    long long page_bytes, int *__restrict__ table, int rec_ints,
-                                    const LoadArgs *__restrict__ args) {
+                                    long long page_bytes, const LoadArgs *__restrict__ args) {
     const int row = blockIdx.x;
     const int r = args->rank;
     if (row < 2 * r) {
@@ -120,19 +122,24 @@ __global__ void load_scatter_kernel(const uint8_t *__restrict__ stage, uint8_t *
         uint4 *dst = reinterpret_cast<uint4 *>(pages + (long long)args->ids[row] * page_bytes);
         for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) dst[i] = src[i];
     }
-    if (row == 0) {
-        int *rec = table + (long long)args->rec_index * rec_ints;
-        for (int i = threadIdx.x; i < 2 * r; i += blockDim.x) rec[kRecHeader + i] = args->ids[i];
-        if (threadIdx.x == 0) {
-            rec[1] = __float_as_int(args->scale);
-            rec[2] = 0;
-            rec[3] = 0;
-            rec[0] = r;
-        }
-    }
 }
 
-__global__ void set_rank_kernel(int *table, long long rec_off, int rank) { table[rec_off] = rank; }
+// One staging slot: the adapter's rows (A_T then B), its LoadArgs, and the
+// table record the load publishes.
+struct StageLayout {
+    size_t args, rec, total;
+};
+constexpr int kStageSlots = 8;
+constexpr size_t kStageRingBytes = (size_t)64 << 20;
+
+StageLayout stage_layout(const lora_pool *p, int rank) {
+    const size_t data = (size_t)2 * rank * p->page_elems * p->esize;
+    StageLayout L;
+    L.args = (data + 255) & ~(size_t)255;
+    L.rec = (L.args + sizeof(LoadArgs) + 255) & ~(size_t)255;
+    L.total = (L.rec + (size_t)p->rec_ints * sizeof(int) + 255) & ~(size_t)255;
+    return L;
+}
 
 }  // namespace lora
 
@@ -264,21 +271,30 @@ int lora_pool_create(lora_pool **out, int dtype, int page_elems, int n_pages, in
     p->d_pages = p->d_table = nullptr;
     p->d_status = nullptr;
     p->h_stage = p->d_stage = nullptr;
-    p->stage_done = nullptr;
     const size_t n_rec = (size_t)max_adapters * n_matrices;
-    p->stage_bytes = (size_t)2 * max_rank * page_elems * p->esize + 256 + sizeof(LoadArgs);
+    p->stage_bytes = stage_layout(p, max_rank).total;
+    // a ring of up to kStageSlots slots, at most about kStageRingBytes of pinned memory (at least 2 slots)
+    p->n_slots = (int)std::max<size_t>(2, std::min<size_t>(kStageSlots, kStageRingBytes / p->stage_bytes));
+    p->next_slot = 0;
     int rc = LORA_OK;
+    try {
+        p->slot_done.assign(p->n_slots, nullptr);
+    } catch (...) {
+        delete p;
+        return LORA_ERR_ARG;
+    }
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaMalloc(&p->d_pages, (size_t)n_pages * page_elems * p->esize) != cudaSuccess ||
         cudaMalloc((void **)&p->d_table, n_rec * p->rec_ints * sizeof(int)) != cudaSuccess ||
         cudaMalloc((void **)&p->d_status, sizeof(int)) != cudaSuccess ||
-        cudaMalloc(&p->d_stage, p->stage_bytes) != cudaSuccess ||
-        cudaMallocHost(&p->h_stage, p->stage_bytes) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p->stage_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaMalloc(&p->d_stage, p->stage_bytes * p->n_slots) != cudaSuccess ||
+        cudaMallocHost(&p->h_stage, p->stage_bytes * p->n_slots) != cudaSuccess ||
         cudaMemset(p->d_table, 0xFF, n_rec * p->rec_ints * sizeof(int)) != cudaSuccess ||   // rank -1
-        cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess)
+        cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess)
         rc = LORA_ERR_CUDA;
+    for (int i = 0; rc == LORA_OK && i < p->n_slots; ++i)
+        if (cudaEventCreateWithFlags(&p->slot_done[i], cudaEventDisableTiming) != cudaSuccess) rc = LORA_ERR_CUDA;
+    if (rc == LORA_OK && cudaDeviceSynchronize() != cudaSuccess) rc = LORA_ERR_CUDA;
     if (rc != LORA_OK) {
         cudaGetLastError();
         lora_pool_destroy(p);
@@ -308,24 +324,104 @@ int lora_pool_destroy(lora_pool *p) {
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_stage) cudaFree(p->d_stage);
     if (p->h_stage) cudaFreeHost(p->h_stage);
-    if (p->stage_done) cudaEventDestroy(p->stage_done);
+    for (cudaEvent_t e : p->slot_done)
+        if (e) cudaEventDestroy(e);
+    for (auto &d : p->deferred)
+        if (d.done) cudaEventDestroy(d.done);
+    for (cudaEvent_t e : p->spare_events) cudaEventDestroy(e);
     cudaGetLastError();
     delete p;
     return LORA_OK;
 }
 
-int lora_pool_free_pages(const lora_pool *p) { return p ? (int)p->free_pages.size() : -1; }
 
-// Frees the pages of record `ri` on the host side (device untouched).
-static void release_pages(lora_pool *p, size_t ri) {
-    int *rec = &p->host_table[ri * p->rec_ints];
-    int r = rec[0];
-    for (int i = 0; i < 2 * r; ++i) p->free_pages.push_back(rec[kRecHeader + i]);
-    rec[0] = -1;
+// Pages of retired records whose event has completed go back to the free list.
+static void reclaim(lora_pool *p) {
+    size_t keep = 0;
+    for (size_t i = 0; i < p->deferred.size(); ++i) {
+        auto &d = p->deferred[i];
+        if (cudaEventQuery(d.done) == cudaSuccess) {
+            for (int pg : d.pages) p->free_pages.push_back(pg);
+            p->spare_events.push_back(d.done);
+        } else {
+            cudaGetLastError();    // cudaErrorNotReady is not an error here
+            if (keep != i) p->deferred[keep] = std::move(d);
+            ++keep;
+        }
+    }
+    p->deferred.resize(keep);
 }
 
-int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale, int h_in, int h_out,
-                   const void *A_T, const void *B, lora_stream stream) {
+// Frees at least `need` pages if the retired ones allow it, waiting for their
+// events oldest first; false if even all of them would not be enough.
+static bool ensure_free(lora_pool *p, size_t need) {
+    reclaim(p);
+    size_t pending = 0;
+    for (auto &d : p->deferred) pending += d.pages.size();
+    if (p->free_pages.size() + pending < need) return false;
+    while (p->free_pages.size() < need && !p->deferred.empty()) {
+        cudaEventSynchronize(p->deferred.front().done);
+        cudaGetLastError();
+        reclaim(p);
+    }
+    return p->free_pages.size() >= need;
+}
+
+static cudaEvent_t take_event(lora_pool *p) {
+    if (!p->spare_events.empty()) {
+        cudaEvent_t e = p->spare_events.back();
+        p->spare_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return e;
+}
+
+// Retires the pages of record `ri` (host mirror marked unloaded).  immediate:
+// straight back to the free list (no kernel can still read them); else they
+// wait for an event recorded now on `st`, after the table update that retired
+// them.
+static int retire_pages(lora_pool *p, size_t ri, bool immediate, cudaStream_t st) {
+    int *rec = &p->host_table[ri * p->rec_ints];
+    const int r = rec[0];
+    rec[0] = -1;
+    if (r <= 0) return LORA_OK;
+    if (immediate) {
+        for (int i = 0; i < 2 * r; ++i) p->free_pages.push_back(rec[kRecHeader + i]);
+        return LORA_OK;
+    }
+    lora_pool::Deferred d;
+    d.done = take_event(p);
+    if (!d.done) return LORA_ERR_CUDA;
+    try {
+        d.pages.assign(rec + kRecHeader, rec + kRecHeader + 2 * r);
+        if (cudaEventRecord(d.done, st) != cudaSuccess) throw 0;
+        p->deferred.push_back(std::move(d));
+    } catch (...) {
+        cudaGetLastError();
+        // the event could not be recorded: wait for the stream instead
+        cudaStreamSynchronize(st);
+        for (int i = 0; i < 2 * r; ++i) p->free_pages.push_back(rec[kRecHeader + i]);
+        p->spare_events.push_back(d.done);
+    }
+    return LORA_OK;
+}
+
+// The next staging slot, once its previous copies have completed.
+static int take_slot(lora_pool *p) {
+    const int slot = p->next_slot;
+    p->next_slot = (slot + 1) % p->n_slots;
+    cudaEventSynchronize(p->slot_done[slot]);   // returns at once for an event never recorded
+    cudaGetLastError();
+    return slot;
+}
+
+static int check_load(const lora_pool *p, int adapter, int matrix, int rank, int h_in, int h_out, const void *A_T,
+                      const void *B) {
     if (!p || adapter < 0 || adapter >= p->max_adapters || matrix < 0 || matrix >= p->n_matrices)
         return LORA_ERR_ARG;
     if (rank < 0 || rank > p->max_rank) return LORA_ERR_RANK;
@@ -334,25 +430,29 @@ int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale,
     if (p->mat_h_in[matrix] >= 0 && (p->mat_h_in[matrix] != h_in || p->mat_h_out[matrix] != h_out))
         return LORA_ERR_SHAPE;
     if (rank > 0 && (!A_T || !B)) return LORA_ERR_ARG;
-    cudaStream_t st = (cudaStream_t)stream;
-    const size_t ri = (size_t)adapter * p->n_matrices + matrix;
-    int *hrec = &p->host_table[ri * p->rec_ints];
-    const int old_rank = hrec[0];
-    if ((int)p->free_pages.size() + (old_rank > 0 ? 2 * old_rank : 0) < 2 * rank) return LORA_ERR_POOL_FULL;
-    if (old_rank >= 0) {
-        // Replacing: queued kernels may still read the old pages.
-        if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
-        release_pages(p, ri);
-    }
+    return LORA_OK;
+}
+
+// Stages one adapter in a slot and enqueues on `st`: the copy of its rows and
+// page ids to the device, the scatter into its pages, the copy of its table
+// record, and the slot's event.  The record copy comes last and is a plain
+// copy, not a kernel, so a kernel launched after it on `st` -- even one that
+// may start before the kernel ahead of it finishes (programmatic dependent
+// launch) -- reads the new record, and the record points at written pages.
+// Pages come from the free list (the caller made room); the host mirror is
+// updated once everything is enqueued.
+static int enqueue_load(lora_pool *p, size_t ri, int adapter, int matrix, int rank, float scale, int h_in, int h_out,
+                        const void *A_T, const void *B, cudaStream_t st, int *slot_out) {
+    const int slot = take_slot(p);
+    const StageLayout L = stage_layout(p, p->max_rank);
+    uint8_t *hs = (uint8_t *)p->h_stage + (size_t)slot * p->stage_bytes;
+    uint8_t *ds = (uint8_t *)p->d_stage + (size_t)slot * p->stage_bytes;
     const int rba = h_in * p->esize, rbb = h_out * p->esize;
-    const size_t data_bytes = (size_t)rank * (rba + rbb);
-    const size_t args_off = (data_bytes + 255) & ~(size_t)255;
-    uint8_t *hs = (uint8_t *)p->h_stage;
     if (rank > 0) {
         std::memcpy(hs, A_T, (size_t)rank * rba);
         std::memcpy(hs + (size_t)rank * rba, B, (size_t)rank * rbb);
     }
-    LoadArgs *la = reinterpret_cast<LoadArgs *>(hs + args_off);
+    LoadArgs *la = reinterpret_cast<LoadArgs *>(hs + L.args);
     la->rec_index = (int)ri;
     la->rank = rank;
     la->scale = scale;
@@ -362,36 +462,131 @@ int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale,
         la->ids[i] = p->free_pages.back();
         p->free_pages.pop_back();
     }
-    const size_t copy_bytes = args_off + offsetof(LoadArgs, ids) + sizeof(int) * 2 * rank;
-    cudaError_t e = cudaMemcpyAsync(p->d_stage, p->h_stage, copy_bytes, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) {
-        const uint8_t *ds = (const uint8_t *)p->d_stage;
-        load_scatter_kernel<<<rank > 0 ? 2 * rank : 1, 256, 0, st>>>(
-            ds, (uint8_t *)p->d_pages, (long long)p->page_elems * p->esize, p->d_table, p->rec_ints,
-            reinterpret_cast<const LoadArgs *>(ds + args_off));
-        count_launch();
-        e = cudaGetLastError();
+    int *hrec_stage = reinterpret_cast<int *>(hs + L.rec);
+    for (int i = 0; i < p->rec_ints; ++i) hrec_stage[i] = -1;
+    hrec_stage[0] = rank;
+    std::memcpy(&hrec_stage[1], &scale, sizeof(int));
+    hrec_stage[2] = hrec_stage[3] = 0;
+    for (int i = 0; i < 2 * rank; ++i) hrec_stage[kRecHeader + i] = la->ids[i];
+    cudaError_t e = cudaSuccess;
+    if (rank > 0) {
+        const size_t data_bytes = (size_t)rank * (rba + rbb);
+        e = cudaMemcpyAsync(ds, hs, data_bytes, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(ds + L.args, hs + L.args, offsetof(LoadArgs, ids) + sizeof(int) * 2 * rank,
+                                cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) {
+            load_scatter_kernel<<<2 * rank, 256, 0, st>>>(ds, (uint8_t *)p->d_pages,
+                                                         (long long)p->page_elems * p->esize,
+                                                         reinterpret_cast<const LoadArgs *>(ds + L.args));
+            count_launch();
+            e = cudaGetLastError();
+        }
     }
-    if (e == cudaSuccess) e = cudaEventRecord(p->stage_done, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->d_table + ri * p->rec_ints, hrec_stage, (size_t)p->rec_ints * sizeof(int),
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(p->slot_done[slot], st);
     if (e != cudaSuccess) {
+        cudaGetLastError();
         for (int i = 2 * rank - 1; i >= 0; --i) p->free_pages.push_back(la->ids[i]);
         return LORA_ERR_CUDA;
     }
-    // The call returns with the adapter resident: the BGMV kernel reads page
-    // tables and pages before it waits on the kernel ahead of it in its
-    // stream, so no load may still be in flight when a kernel is launched.
-    if (cudaEventSynchronize(p->stage_done) != cudaSuccess) {
-        for (int i = 2 * rank - 1; i >= 0; --i) p->free_pages.push_back(la->ids[i]);
-        return LORA_ERR_CUDA;
-    }
-    hrec[0] = rank;
-    std::memcpy(&hrec[1], &scale, sizeof(int));
-    for (int i = 0; i < 2 * rank; ++i) hrec[kRecHeader + i] = la->ids[i];
+    int *hrec = &p->host_table[ri * p->rec_ints];
+    std::memcpy(hrec, hrec_stage, (size_t)p->rec_ints * sizeof(int));
     p->mat_h_in[matrix] = h_in;
     p->mat_h_out[matrix] = h_out;
     if (adapter + 1 > p->mat_n_ids[matrix]) p->mat_n_ids[matrix] = adapter + 1;
     if (rank > p->mat_max_rank[matrix]) p->mat_max_rank[matrix] = rank;
+    if (slot_out) *slot_out = slot;
     return LORA_OK;
+}
+
+int lora_pool_free_pages(const lora_pool *p) {
+    if (!p) return -1;
+    reclaim(const_cast<lora_pool *>(p));
+    return (int)p->free_pages.size();
+}
+
+int lora_pool_load(lora_pool *p, int adapter, int matrix, int rank, float scale, int h_in, int h_out,
+                   const void *A_T, const void *B, lora_stream stream) {
+    int rc = check_load(p, adapter, matrix, rank, h_in, h_out, A_T, B);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t ri = (size_t)adapter * p->n_matrices + matrix;
+    const int old_rank = p->host_table[ri * p->rec_ints];
+    reclaim(p);
+    size_t pending = 0;
+    for (auto &d : p->deferred) pending += d.pages.size();
+    if (p->free_pages.size() + pending + (old_rank > 0 ? 2 * old_rank : 0) < (size_t)2 * rank)
+        return LORA_ERR_POOL_FULL;
+    if (old_rank >= 0) {
+        // Replacing: queued kernels may still read the old pages.
+        if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
+        retire_pages(p, ri, true, st);
+    }
+    if (!ensure_free(p, (size_t)2 * rank)) return LORA_ERR_POOL_FULL;
+    int slot = 0;
+    if ((rc = enqueue_load(p, ri, adapter, matrix, rank, scale, h_in, h_out, A_T, B, st, &slot))) return rc;
+    // The call returns with the adapter resident, for kernels on any stream.
+    if (cudaEventSynchronize(p->slot_done[slot]) != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    return LORA_OK;
+}
+
+int lora_pool_load_async(lora_pool *p, int adapter, int matrix, int rank, float scale, int h_in, int h_out,
+                         const void *A_T, const void *B, lora_stream stream) {
+    int rc = check_load(p, adapter, matrix, rank, h_in, h_out, A_T, B);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t ri = (size_t)adapter * p->n_matrices + matrix;
+    const int old_rank = p->host_table[ri * p->rec_ints];
+    reclaim(p);
+    size_t pending = 0;
+    for (auto &d : p->deferred) pending += d.pages.size();
+    // the replaced adapter's pages are retired on `st` after the new record is
+    // published, so they cannot serve this load
+    if (p->free_pages.size() + pending < (size_t)2 * rank) return LORA_ERR_POOL_FULL;
+    if (!ensure_free(p, (size_t)2 * rank)) return LORA_ERR_POOL_FULL;
+    std::vector<int> old;
+    if (old_rank > 0) {
+        const int *hrec = &p->host_table[ri * p->rec_ints];
+        old.assign(hrec + kRecHeader, hrec + kRecHeader + 2 * old_rank);
+    }
+    if ((rc = enqueue_load(p, ri, adapter, matrix, rank, scale, h_in, h_out, A_T, B, st, nullptr))) return rc;
+    if (!old.empty()) {
+        lora_pool::Deferred d;
+        d.done = take_event(p);
+        if (!d.done || cudaEventRecord(d.done, st) != cudaSuccess) {
+            cudaGetLastError();
+            cudaStreamSynchronize(st);
+            for (int pg : old) p->free_pages.push_back(pg);
+            if (d.done) p->spare_events.push_back(d.done);
+        } else {
+            d.pages = std::move(old);
+            p->deferred.push_back(std::move(d));
+        }
+    }
+    return LORA_OK;
+}
+
+int lora_pool_prefetch(lora_pool *p, const lora_adapter_src *list, int n, lora_stream stream) {
+    if (!p || n < 0 || (n > 0 && !list)) return LORA_ERR_ARG;
+    int enqueued = 0;
+    for (int i = 0; i < n; ++i) {
+        const lora_adapter_src &e = list[i];
+        if (e.adapter < 0 || e.adapter >= p->max_adapters || e.matrix < 0 || e.matrix >= p->n_matrices)
+            return LORA_ERR_ARG;
+        const size_t ri = (size_t)e.adapter * p->n_matrices + e.matrix;
+        if (p->host_table[ri * p->rec_ints] >= 0) continue;      // already resident
+        const int rc = lora_pool_load_async(p, e.adapter, e.matrix, e.rank, e.scale, e.h_in, e.h_out, e.A_T, e.B,
+                                            stream);
+        if (rc) return rc;
+        ++enqueued;
+    }
+    return enqueued;
 }
 
 int lora_pool_unload(lora_pool *p, int adapter, int matrix) {
@@ -400,11 +595,34 @@ int lora_pool_unload(lora_pool *p, int adapter, int matrix) {
     const size_t ri = (size_t)adapter * p->n_matrices + matrix;
     if (p->host_table[ri * p->rec_ints] < 0) return LORA_ERR_NOT_LOADED;
     if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
-    set_rank_kernel<<<1, 1>>>(p->d_table, (long long)ri * p->rec_ints, -1);
-    count_launch();
-    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
-    release_pages(p, ri);
+    const int minus1 = -1;
+    if (cudaMemcpy(p->d_table + ri * p->rec_ints, &minus1, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    retire_pages(p, ri, true, nullptr);
+    reclaim(p);
     return LORA_OK;
+}
+
+int lora_pool_unload_async(lora_pool *p, int adapter, int matrix, lora_stream stream) {
+    if (!p || adapter < 0 || adapter >= p->max_adapters || matrix < 0 || matrix >= p->n_matrices)
+        return LORA_ERR_ARG;
+    const size_t ri = (size_t)adapter * p->n_matrices + matrix;
+    if (p->host_table[ri * p->rec_ints] < 0) return LORA_ERR_NOT_LOADED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int slot = take_slot(p);
+    int *hrank = reinterpret_cast<int *>((uint8_t *)p->h_stage + (size_t)slot * p->stage_bytes +
+                                         stage_layout(p, p->max_rank).rec);
+    *hrank = -1;
+    if (cudaMemcpyAsync(p->d_table + ri * p->rec_ints, hrank, sizeof(int), cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaEventRecord(p->slot_done[slot], st) != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    return retire_pages(p, ri, false, st);
 }
 
 int lora_get_error(lora_pool *p, int *device_status) {

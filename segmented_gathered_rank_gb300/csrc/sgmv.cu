@@ -1,6 +1,6 @@
-// SGMV for prefill: "segmented gather, for contiguous segments of tokens
-// sharing an adapter" ("Multi-LoRA Serving", section "The kernel trick:
-// gather, do not merge"), with per-adapter ranks (S-LoRA slide 10, MBGMM).
+// SGMV for prefill: the gathered low-rank product over runs of consecutive
+// tokens that share one adapter ("Multi-LoRA Serving", section "The kernel
+// trick: gather, do not merge"), with per-adapter ranks (S-LoRA slide 10, MBGMM).
 //
 //   shrink:  v[t][j]  = sum_k x[t][k] * A_T_a[j][k]            j < r_a
 //   expand:  y[t][n] += s_a * sum_j v[t][j] * B_a[j][n]

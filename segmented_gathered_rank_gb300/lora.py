@@ -42,7 +42,8 @@ EXPORTS = ["lora_pool_create", "lora_pool_destroy", "lora_pool_load", "lora_pool
            "lora_pool_free_pages", "lora_sgmv_shrink", "lora_sgmv_expand", "lora_bgmv",
            "lora_layer_forward_workspace_size", "lora_layer_forward", "lora_get_error", "lora_strerror",
            "lora_launch_count", "lora_layer_forward_noalloc", "lora_tier_cache_create", "lora_tier_cache_destroy",
-           "lora_tier_cache_touch", "lora_tier_cache_resident", "lora_tier_sim"]
+           "lora_tier_cache_touch", "lora_tier_cache_resident", "lora_tier_sim", "lora_pool_load_async",
+           "lora_pool_unload_async", "lora_pool_prefetch"]
 
 if not os.path.exists(_build.LIB):
     raise ImportError(f"CUDA library {_build.LIB} is not built: run segmented_gathered_rank_gb300.build.build()")
@@ -75,6 +76,17 @@ _sig("lora_layer_forward_noalloc", _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P)
 _sig("lora_get_error", _I, _P, ctypes.POINTER(_I))
 _sig("lora_strerror", ctypes.c_char_p, _I)
 _sig("lora_launch_count", ctypes.c_ulonglong)
+
+
+class AdapterSrc(ctypes.Structure):
+    """``lora_adapter_src``: one entry of a prefetch list."""
+    _fields_ = [("adapter", _I), ("matrix", _I), ("rank", _I), ("scale", ctypes.c_float), ("h_in", _I),
+                ("h_out", _I), ("A_T", _P), ("B", _P)]
+
+
+_sig("lora_pool_load_async", _I, _P, _I, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P)
+_sig("lora_pool_unload_async", _I, _P, _I, _I, _P)
+_sig("lora_pool_prefetch", _I, _P, ctypes.POINTER(AdapterSrc), _I, _P)
 _sig("lora_tier_cache_create", _I, ctypes.POINTER(_P), _I, _I, _I)
 _sig("lora_tier_cache_destroy", _I, _P)
 _sig("lora_tier_cache_touch", _I, _P, _I, ctypes.POINTER(_I))
@@ -157,6 +169,31 @@ def lora_pool_load(pool, adapter: int, matrix: int, rank: int, scale: float, h_i
 
 def lora_pool_unload(pool, adapter: int, matrix: int) -> None:
     _check(_lib.lora_pool_unload(pool, adapter, matrix), "lora_pool_unload")
+
+
+def lora_pool_load_async(pool, adapter: int, matrix: int, rank: int, scale: float, h_in: int, h_out: int,
+                         A_T, B, stream=None) -> None:
+    """Enqueue an upload on ``stream`` and return (the host arrays are copied
+    before the call returns)."""
+    _check(_lib.lora_pool_load_async(pool, adapter, matrix, rank, float(scale), h_in, h_out, _hptr(A_T), _hptr(B),
+                                     _stream(stream)), "lora_pool_load_async")
+
+
+def lora_pool_unload_async(pool, adapter: int, matrix: int, stream=None) -> None:
+    _check(_lib.lora_pool_unload_async(pool, adapter, matrix, _stream(stream)), "lora_pool_unload_async")
+
+
+def lora_pool_prefetch(pool, entries, stream=None) -> int:
+    """Upload every (adapter, matrix, rank, scale, h_in, h_out, A_T, B) entry not
+    resident yet; returns how many uploads were enqueued."""
+    entries = list(entries)
+    arr = (AdapterSrc * max(1, len(entries)))()
+    for i, (a, m, r, sc, hi, ho, at, b) in enumerate(entries):
+        arr[i] = AdapterSrc(a, m, r, float(sc), hi, ho, _hptr(at), _hptr(b))
+    rc = _lib.lora_pool_prefetch(pool, arr, len(entries), _stream(stream))
+    if rc < 0:
+        raise LoraError(rc, "lora_pool_prefetch")
+    return int(rc)
 
 
 def lora_pool_free_pages(pool) -> int:

@@ -87,3 +87,12 @@ def test_strerror_covers_every_code(lib):
     texts = [L.lora_strerror(c) for c in codes]
     assert len(set(texts)) == len(texts) and "unknown status" not in texts
     assert L.lora_strerror(12345) == "unknown status"
+
+
+def test_async_upload_host_checks(lib):
+    from segmented_gathered_rank_gb300 import lora as L
+    z = ctypes.c_void_p(0)
+    assert L._lib.lora_pool_load_async(None, 0, 0, 4, 1.0, 8, 8, None, None, z) == L.LORA_ERR_ARG
+    assert L._lib.lora_pool_unload_async(None, 0, 0, z) == L.LORA_ERR_ARG
+    assert L._lib.lora_pool_prefetch(None, None, 0, z) == L.LORA_ERR_ARG
+
