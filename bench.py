@@ -20,6 +20,8 @@ Workloads (``--workload``; default ``fused_layer``):
                       expand on q, k, v, o.
   encoder_mixed_rank  16384 tokens (128 x 128), 1024 adapters of ranks 8..64,
                       a step is shrink + expand on all 48 projections.
+  fused_layer_fp8     fused_layer with an FP8 (e4m3) base product:
+                      lora_layer_forward_fp8 on q, k, v, o.
 
 The prefill and encoder lines carry a second roofline object,
 ``shrink_roofline``, for the shrink kernel (the expand is the first).
@@ -95,6 +97,7 @@ KERNEL_SOURCES = {
     "encoder_mixed_rank": ("sgmv.cu", "internal.cuh"),
     "encoder_mixed_rank.shrink": ("sgmv.cu", "internal.cuh"),
     "fused_layer": None,
+    "fused_layer_fp8": None,
 }
 
 
@@ -588,10 +591,73 @@ class FusedLayer(Runner):
         return units / t_total, f"{n} projections x 32 sampled tokens (oracle.layer with base), {t_total:.1f} s"
 
 
+class FusedLayerFp8(FusedLayer):
+    """The fused layer with an FP8 base product (lora_layer_forward_fp8): W held
+    as e4m3 codes with a per-tensor scale, x quantised per row inside the call,
+    adapters in bf16."""
+    name = "fused_layer_fp8"
+
+    @staticmethod
+    def describe(layers: int = 32) -> str:
+        return ("fused_layer_fp8: as fused_layer, base weights e4m3 (per-tensor scale), x quantised per row to "
+                "e4m3 inside the call, adapters bf16; step = lora_layer_forward_fp8 on q,k,v,o")
+
+    def __init__(self, seed: int = 0):
+        super().__init__(seed)
+        torch, w, L = self.torch, self.w, self.L
+        self.W8, self.s_w = [], []
+        for m in range(4):
+            codes, s_w = w.W_e4m3(m)
+            self.W8.append(torch.from_numpy(codes).cuda())
+            self.s_w.append(s_w)
+        self.W = None
+        self.ws_bytes = max(L.lora_layer_forward_fp8_workspace_size(self.pool.handle, m, w.S, w.T) for m in range(4))
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.dominant = dict(self.dominant, name="lora_layer_forward_fp8 (quantise x + FP8 base GEMM + adapter term)",
+                             peak_key="fp8")
+        self.config = dict(self.config, workload=self.describe())
+
+    def step(self, stream=None):
+        w, L = self.w, self.L
+        for m in range(4):
+            L.lora_layer_forward_fp8(self.pool.handle, m, self._x(m), self.W8[m], self.s_w[m], self.y[m], self.ss,
+                                     self.sa, w.S, w.T, self.ws, self.ws_bytes, stream)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle
+        from oracle import fp8 as F
+        w = self.w
+        tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+        rng = np.random.default_rng(0)
+        xs = {0: w.x(0), 3: w.x(3)}
+        units, t_total, n = 0, 0.0, 0
+        cache = self.__dict__.setdefault("_cpu_cache_fp8", {})
+        while True:
+            m = n % 4
+            if m not in cache:
+                cache[m] = (oracle.adapters_for(w, m), w.W_e4m3(m))
+            ad, (codes, s_w) = cache[m]
+            rows = np.sort(rng.choice(w.T, 8, replace=False)).astype(np.int32)
+            x = xs[0 if m < 3 else 3]
+            t0 = time.perf_counter()
+            q, sx = F.quantize_rows(x[rows])
+            base = F.base(q, sx, codes, s_w)
+            delta, _ = oracle.layer(x, None, tok, ad, w.matrices[m].h_out, rows=rows)
+            _ = base + delta
+            t_total += time.perf_counter() - t0
+            units += len(rows)
+            n += 1
+            if t_total >= budget_s:
+                break
+        return units / t_total, f"{n} projections x 8 sampled tokens (oracle: FP8 base + bf16 adapter term), " \
+                                f"{t_total:.1f} s"
+
+
 RUNNERS = {"decode_bgmv": DecodeBGMV, "prefill_sgmv": PrefillSGMV, "encoder_mixed_rank": EncoderMixedRank,
-           "fused_layer": FusedLayer}
+           "fused_layer": FusedLayer, "fused_layer_fp8": FusedLayerFp8}
 
 DTYPE = "bf16"
+DTYPES = {"fused_layer_fp8": "e4m3 base, bf16 adapters"}
 
 
 # ----------------------------------------------------------------------------
@@ -605,7 +671,8 @@ def run_reference(args, dist: Dist):
     cls = RUNNERS[args.workload]
     r = cls.__new__(cls)          # only the generator side: no device state
     r.w = {"decode_bgmv": lambda: I.decode_bgmv(layers=32), "prefill_sgmv": I.prefill_sgmv,
-           "encoder_mixed_rank": I.encoder_mixed_rank, "fused_layer": I.fused_layer}[args.workload]()
+           "encoder_mixed_rank": I.encoder_mixed_rank, "fused_layer": I.fused_layer,
+           "fused_layer_fp8": I.fused_layer}[args.workload]()
     r.T = r.w.T
     r.layers = 32
     r.h = r.w.matrices[0].h_in
@@ -701,9 +768,16 @@ def run_ours(args, dist: Dist):
             d1.record(stream)
         torch.cuda.synchronize()
         per_launch_s = d0.elapsed_time(d1) / 1e3 / (args.steps * spec["launches_per_step"])
+        note = None
         if spec["bound"] == "hbm":
             achieved = spec["work_per_launch"] / per_launch_s / 1e9
             peak = peaks["hbm_gbs"]
+        elif spec.get("peak_key") == "fp8":
+            # no FP8 rate is measured on this machine: the measured bf16 rate times the
+            # nominal dense FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+            achieved = spec["work_per_launch"] / per_launch_s / 1e12
+            peak = peaks["bf16_tflops"] * 2.0
+            note = "FP8 peak = measured bf16 burst x 2 (nominal dense ratio)"
         else:
             achieved = spec["work_per_launch"] / per_launch_s / 1e12
             peak = peaks["bf16_tflops"]
@@ -714,7 +788,8 @@ def run_ours(args, dist: Dist):
         return {"bound": spec["bound"], "achieved": achieved, "peak": peak, "unit": spec["unit"],
                 "frac": achieved / peak, "traffic": traffic, "kernel": spec["name"],
                 "work_per_launch": spec["work_per_launch"], "launch_us": per_launch_s * 1e6,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src}
+                "peak_source": (f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src) +
+                               (f"; {note}" if note else "")}
 
     roof = roofline(runner.dominant, g_dom, args.workload)
     extra = {}
@@ -748,7 +823,7 @@ def run_ours(args, dist: Dist):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
+            "vs_baseline": None, "dtype": DTYPES.get(args.workload, DTYPE), "data": "synthetic",
             "config": {**runner.config, "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single"},
             "roofline": roof,
             **extra,

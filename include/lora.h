@@ -266,6 +266,42 @@ int lora_layer_forward_noalloc(lora_pool *pool, int matrix, const void *x, const
                                lora_stream stream);
 
 /*
+ * FP8 base ("Multi-LoRA Serving - S-LoRA/Punica Batching, Adapter Hot-Swap &
+ * Memory", the failure assumptions and "Operating it": the base may run in
+ * FP8 while adapters trained on a bf16 base keep working in bf16).
+ *
+ * lora_quantize_e4m3: per-row quantisation of x (T x h bf16, device, h a
+ * multiple of 8) to e4m3 codes q (T x h bytes, device, 8-byte aligned) and
+ * fp32 scales sx (T, device):
+ *   sx[t] = max_k |x[t][k]| / 448  (fp32 division; 1 for a row of zeros),
+ *   q[t][k] = e4m3(x[t][k] / sx[t])  (fp32 division; round to nearest even,
+ *             saturating at +-448; e4m3 = 1 sign, 4 exponent bits with bias
+ *             7, 3 mantissa bits, no infinities).
+ * Errors: LORA_ERR_ARG.
+ */
+int lora_quantize_e4m3(const void *x, int T, int h, void *q, float *sx, lora_stream stream);
+
+/* Workspace lora_layer_forward_fp8 needs: lora_layer_forward's plus the
+ * codes and scales of x (0 on a bad argument). */
+size_t lora_layer_forward_fp8_workspace_size(const lora_pool *pool, int matrix, int S, int T);
+
+/*
+ * lora_layer_forward with an FP8 base product:
+ *   y[t][n] = sx[t] * w_scale * sum_k q[t][k] * W8[n][k]
+ *           + scale_a * sum_j (sum_k x[t][k] A_T_a[j][k]) B_a[j][n]
+ * W8: h_out x h_in e4m3 codes (device, the base weight quantised by the
+ * caller with the per-tensor scale w_scale > 0); x: bf16 as for
+ * lora_layer_forward -- quantised here per row (lora_quantize_e4m3) for the
+ * base product, used unquantised for the low-rank term.  The base product
+ * runs on the tensor cores (kind::f8f6f4), so the pool must be bf16, h_in a
+ * multiple of 128 and h_out a multiple of 32 (else LORA_ERR_SHAPE).  y is
+ * overwritten.  Workspace, streams and errors as lora_layer_forward.
+ */
+int lora_layer_forward_fp8(lora_pool *pool, int matrix, const void *x, const void *W8, float w_scale, void *y,
+                           const int *seg_starts, const int *seg_adapter, int S, int T,
+                           void *workspace, size_t ws_bytes, lora_stream stream);
+
+/*
  * Synchronise the device, read the pool's device status word into
  * *device_status (may be NULL), and clear it.  Returns LORA_OK when the word
  * was zero, LORA_ERR_DEVICE_INDEX when any LORA_DEV_* bit was set, or

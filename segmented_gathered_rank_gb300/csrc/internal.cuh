@@ -288,12 +288,23 @@ int num_sms();   // SMs of the current device (cached per device)
 // once per device and kernel; thread safe).  occupancy (optional): resident
 // CTAs per SM of `threads` threads at that size.  LORA_OK or LORA_ERR_CUDA.
 int smem_optin(const void *func, size_t bytes, int threads = 0, int *occupancy = nullptr);
-bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T);
+// The FP8 base product: x quantised per row (codes xq [T x h_in], scales sx [T]) against
+// W given as e4m3 codes with one scale w_scale; see lora_layer_forward_fp8.
+struct Fp8Base {
+    const void *xq;
+    const float *sx;
+    float w_scale;
+    bool quantize;      // the layer call writes xq and sx from x itself (before its GEMM)
+};
+// Per-row e4m3 codes and scales of x (see lora_quantize_e4m3).
+int launch_quantize(const void *x, int T, int h, void *q, float *sx, cudaStream_t st);
+bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T, bool fp8 = false);
 // tile_ad != nullptr: M-tiles with tile_ad[m] >= 0 also get that adapter's term
-// s * v . B (v: T x ld_v fp32) inside the GEMM.
+// s * v . B (v: T x ld_v fp32) inside the GEMM.  f8 != nullptr: W holds e4m3 codes and
+// the base product is the FP8 one.
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
                    cudaStream_t st, int matrix = 0, const int *tile_ad = nullptr, const float *v = nullptr,
-                   int ld_v = 0);
+                   int ld_v = 0, const Fp8Base *f8 = nullptr);
 // Tensor-core shrink (tcgen05) of 128-row tiles that share one adapter of
 // rank 1..kFuseMaxRank: the fused layer's uniform M-tiles (tile_ad), or, for
 // a segment table, 128-row pieces of the segments with at least
@@ -309,8 +320,10 @@ constexpr int kShrinkTcMaxS = 8192;
 bool shrink_tc_ok(const lora_pool *pool, int h_in, int S);
 int launch_shrink_tc(const lora_pool *pool, int matrix, int h_in, const void *x, int T, int *tile_ad,
                      const int *seg_starts, const int *seg_adapter, int S, float *v, int ld_v, cudaStream_t st);
+// f8 != nullptr: the base product is the FP8 one (W holds e4m3 codes; tensor cores required).
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
-                       const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st);
+                       const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st,
+                       const Fp8Base *f8 = nullptr);
 int launch_base_gemm(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y,
                      int T, cudaStream_t st);
 

@@ -42,6 +42,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreadsTC = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);   // FP8 base: K-blocks of 128 e4m3 (the same 128 bytes)
 
 // The fused tile's low-rank term enters the accumulator in rounds of kRound ranks,
 // staged K-major with 64-byte swizzling; 32-rank rounds keep the operands at
@@ -62,6 +63,10 @@ struct LayerTcParams {
     int m;
     const float *v;         // [T][ld_v]: x . A_a of the fused tiles' rows
     int ld_v;
+    // FP8 base (FP8 variant): the accumulator holds sum_k q[t][k] W8[n][k]; row t is
+    // scaled by sx[t] * w_scale, and the fused tiles' low-rank operand enters divided by it
+    const float *sx;
+    float w_scale;
 };
 
 template <int ST>
@@ -171,7 +176,7 @@ __device__ __forceinline__ void load_round(const LayerTcParams &p, int tile, int
 // Writes the round's operands; returns the tile's number of rounds.
 template <int ST>
 __device__ int store_round(const FillCache &fc, int round, const RoundRegs &g, uint8_t *a2hi, uint8_t *a2lo,
-                           uint8_t *b2, Ctrl<ST> *ctrl, int ethr) {
+                           uint8_t *b2, Ctrl<ST> *ctrl, int ethr, float row_mul) {
     const int lane = ethr & 31, w = ethr >> 5;
     const int rounds = (fc.r + kRound - 1) / kRound;
     const int j0 = round * kRound, rn = max(0, min(kRound, fc.r - j0));
@@ -181,7 +186,7 @@ __device__ int store_round(const FillCache &fc, int round, const RoundRegs &g, u
         if (round == 0) ctrl->arounds = rounds;
     }
     if (kpad == 0) return rounds;
-    const float s = fc.s;
+    const float s = fc.s * row_mul;
 #pragma unroll
     for (int c = 0; c < kRound / 8; ++c) {
         if (c * 8 >= kpad) break;
@@ -221,7 +226,7 @@ __device__ __forceinline__ void give_up(Ctrl<ST> *c, int *status) {
     flag(status, LORA_DEV_WAIT_TIMEOUT);
 }
 
-template <int STAGES, bool FUSE>
+template <int STAGES, bool FUSE, bool FP8>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     layer_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                          LayerTcParams p) {
@@ -279,8 +284,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     mbar_arrive_expect_tx(&ctrl->full[stage], STAGE_BYTES);
-                    tma_load_2d(sa, &tmx, kb * BK, mb * BM, &ctrl->full[stage]);
-                    tma_load_2d(sa + A_BYTES, &tmw, kb * BK, nb * BN, &ctrl->full[stage]);
+                    const int kx = kb * (FP8 ? 2 * BK : BK);      // K-block origin in elements (128 bytes)
+                    tma_load_2d(sa, &tmx, kx, mb * BM, &ctrl->full[stage]);
+                    tma_load_2d(sa + A_BYTES, &tmw, kx, nb * BN, &ctrl->full[stage]);
                     last_par[stage] = (int)phase;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -321,9 +327,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        mma_bf16(d, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), IDESC,
-                                 (kb | k) != 0);
+                    for (int k = 0; k < 4; ++k) {      // 32 bytes of K per MMA: 16 bf16 or 32 e4m3
+                        if (FP8)
+                            mma_f8(d, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), IDESC_F8,
+                                   (kb | k) != 0);
+                        else
+                            mma_bf16(d, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), IDESC,
+                                     (kb | k) != 0);
+                    }
                     mma_commit(&ctrl->empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -369,6 +380,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             FillCache fc;
             RoundRegs g;
             lookup_adapter(p, t, lane, fc);
+            float row_mul = 1.f;       // FP8: the accumulator is in units of sx[row] * w_scale
+            if (FP8) {
+                const int row = (t % p.num_m) * BM + ethr;
+                row_mul = 1.f / ((row < p.T ? p.sx[row] : 1.f) * p.w_scale);
+            }
             const int rounds = max(1, (fc.r + kRound - 1) / kRound);
             load_round(p, t, 0, fc, ethr, g);
             for (int rd = 0; rd < rounds; ++rd) {
@@ -380,7 +396,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         return;
                     }
                 }
-                store_round<STAGES>(fc, rd, g, a2hi, a2lo, b2, ctrl, ethr);
+                store_round<STAGES>(fc, rd, g, a2hi, a2lo, b2, ctrl, ethr, row_mul);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctrl->aready);
@@ -400,6 +416,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             fence_after_sync();
             const int mb = tile % p.num_m, nb = tile / p.num_m;
             const int row = mb * BM + sub * 32 + lane;
+            const float out_mul = FP8 && row < p.T ? p.sx[row] * p.w_scale : 1.f;
 
             for (int c = 0; c < BN / 32; ++c) {
                 const int col0 = nb * BN + c * 32;
@@ -407,6 +424,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 __syncwarp();
                 tmem_ld32(tmem + (uint32_t)(b * BN + c * 32) + ((uint32_t)(sub * 32) << 16), f);
                 if (col0 >= p.N || row >= p.T) continue;
+                if (FP8) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] *= out_mul;
+                }
                 uint4 *dst = reinterpret_cast<uint4 *>(p.y + (long long)row * p.N + col0);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -873,35 +894,55 @@ bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t oute
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int ST, bool FUSE>
+// 2-D byte tensor [outer x inner] (e4m3 codes), box [box_outer x 128], 128-byte swizzle:
+// the same 128-byte rows as the bf16 maps.
+bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {(cuuint32_t)(2 * BK), box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int ST, bool FUSE, bool FP8>
 int launch_gemm_variant(const CUtensorMap &tmx, const CUtensorMap &tmw, const LayerTcParams &p, cudaStream_t st) {
     const size_t smem = (size_t)ST * STAGE_BYTES + (FUSE ? 2 * A2_BYTES + B2_BYTES : 0) + sizeof(Ctrl<ST>) + 1024;
-    if (smem_optin(reinterpret_cast<const void *>(layer_gemm_tc_kernel<ST, FUSE>), smem)) return LORA_ERR_CUDA;
+    if (smem_optin(reinterpret_cast<const void *>(layer_gemm_tc_kernel<ST, FUSE, FP8>), smem)) return LORA_ERR_CUDA;
     const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-    layer_gemm_tc_kernel<ST, FUSE><<<grid, kThreadsTC, smem, st>>>(tmx, tmw, p);
+    layer_gemm_tc_kernel<ST, FUSE, FP8><<<grid, kThreadsTC, smem, st>>>(tmx, tmw, p);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
 
-bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T) {
-    return pool->dtype == LORA_BF16 && h_in % BK == 0 && h_out % 32 == 0 && T > 0 && encode_fn() != nullptr &&
-           num_sms() > 0;
+bool gemm_tc_ok(const lora_pool *pool, int h_in, int h_out, int T, bool fp8) {
+    return pool->dtype == LORA_BF16 && h_in % (fp8 ? 2 * BK : BK) == 0 && h_out % 32 == 0 && T > 0 &&
+           encode_fn() != nullptr && num_sms() > 0;
 }
 
 int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, const void *W, void *y, int T,
-                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v) {
+                   cudaStream_t st, int matrix, const int *tile_ad, const float *v, int ld_v, const Fp8Base *f8) {
     CUtensorMap tmx, tmw;
-    if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM) || !make_tmap(&tmw, W, (uint64_t)h_in, (uint64_t)h_out, BN))
+    if (f8) {
+        if (!make_tmap_u8(&tmx, f8->xq, (uint64_t)h_in, (uint64_t)T, BM) ||
+            !make_tmap_u8(&tmw, W, (uint64_t)h_in, (uint64_t)h_out, BN))
+            return LORA_ERR_CUDA;
+    } else if (!make_tmap(&tmx, x, (uint64_t)h_in, (uint64_t)T, BM) ||
+               !make_tmap(&tmw, W, (uint64_t)h_in, (uint64_t)h_out, BN)) {
         return LORA_ERR_CUDA;
+    }
     LayerTcParams p;
     p.T = T;
     p.N = h_out;
     p.K = h_in;
     p.num_m = (T + BM - 1) / BM;
     p.num_n = (h_out + BN - 1) / BN;
-    p.num_k = h_in / BK;
+    p.num_k = h_in / (f8 ? 2 * BK : BK);
     p.num_tiles = p.num_m * p.num_n;
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.status = pool->d_status;
@@ -910,8 +951,14 @@ int launch_gemm_tc(const lora_pool *pool, int h_in, int h_out, const void *x, co
     p.m = matrix;
     p.v = v;
     p.ld_v = ld_v;
-    if (tile_ad) return launch_gemm_variant<4, true>(tmx, tmw, p, st);
-    return launch_gemm_variant<4, false>(tmx, tmw, p, st);
+    p.sx = f8 ? f8->sx : nullptr;
+    p.w_scale = f8 ? f8->w_scale : 1.f;
+    if (f8) {
+        if (tile_ad) return launch_gemm_variant<4, true, true>(tmx, tmw, p, st);
+        return launch_gemm_variant<4, false, true>(tmx, tmw, p, st);
+    }
+    if (tile_ad) return launch_gemm_variant<4, true, false>(tmx, tmw, p, st);
+    return launch_gemm_variant<4, false, false>(tmx, tmw, p, st);
 }
 
 bool shrink_tc_ok(const lora_pool *pool, int h_in, int S) {

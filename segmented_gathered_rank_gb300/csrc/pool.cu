@@ -150,8 +150,8 @@ namespace lora {
 // join become graph edges.
 struct SideStream {
     int device = -1;
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaStream_t s = nullptr, s2 = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
 };
 
 static SideStream *side_stream() {
@@ -162,8 +162,10 @@ static SideStream *side_stream() {
         // a stream of another device stays as it is: work of this thread may still use it
         SideStream n;
         if (cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&n.s2, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.join2, cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
         n.device = dev;
         ss = n;
@@ -175,9 +177,18 @@ static SideStream *side_stream() {
 // the whole batch (tensor cores when the shape allows), then each token's own
 // low-rank term: shrink into v, expand into y.
 int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, const void *x, const void *W, void *y,
-                       const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st) {
+                       const int *seg_starts, const int *seg_adapter, int S, int T, float *v, cudaStream_t st,
+                       const Fp8Base *f8) {
     int rc;
-    const bool tc = gemm_tc_ok(p, h_in, h_out, T);
+    const bool tc = gemm_tc_ok(p, h_in, h_out, T, f8 != nullptr);
+    if (f8 && !tc) return LORA_ERR_SHAPE;      // the FP8 base product runs on the tensor cores only
+    // FP8: x's codes and scales, before the GEMM -- on the call's stream, or (tensor-core
+    // tiles, below) on a second side stream beside the tensor-core shrink
+    const bool q_side = f8 && f8->quantize && shrink_tc_ok(p, h_in, S) &&
+                        sgmv_plan_ok(p, matrix, S, T, true) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S);
+    if (f8 && f8->quantize && !q_side && (rc = launch_quantize(x, T, h_in, const_cast<void *>(f8->xq),
+                                                               const_cast<float *>(f8->sx), st)))
+        return rc;
     const bool tcs = tc && shrink_tc_ok(p, h_in, S);
     if (sgmv_plan_ok(p, matrix, S, T, tcs) && sgmv_shrink_ok(p, h_in, S) && sgmv_expand_ok(p, h_out, S)) {
         // With tensor-core tiles (tcs):
@@ -199,7 +210,8 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
             if ((rc = launch_sgmv_plan(p, matrix, seg_starts, seg_adapter, S, T, plan, st))) return rc;
             if ((rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st)))
                 return rc;
-            rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st) : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+            rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, 0, nullptr, nullptr, 0, f8)
+                    : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
             if (rc) return rc;
             return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st);
         }
@@ -207,6 +219,19 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
         SideStream *side = side_stream();
         cudaStream_t st3 = st;
         if (side && cudaEventRecord(side->fork, st) != cudaSuccess) return LORA_ERR_CUDA;
+        if (q_side) {   // FP8: x quantised on the second side stream, joined before the GEMM
+            cudaStream_t sq = side ? side->s2 : st;
+            if (side && cudaStreamWaitEvent(sq, side->fork, 0) != cudaSuccess) return LORA_ERR_CUDA;
+            rc = launch_quantize(x, T, h_in, const_cast<void *>(f8->xq), const_cast<float *>(f8->sx), sq);
+            if (side && cudaEventRecord(side->join2, sq) != cudaSuccess) {
+                cudaStreamWaitEvent(st, side->join2, 0);
+                return LORA_ERR_CUDA;
+            }
+            if (rc) {
+                if (side) cudaStreamWaitEvent(st, side->join2, 0);   // no side work is left unjoined
+                return rc;
+            }
+        }
         // the tensor-core shrink is enqueued first, so its CTAs take the SMs first
         rc = launch_shrink_tc(p, matrix, h_in, x, T, tile_ad, seg_starts, seg_adapter, S, v, p->max_rank, st);
         if (side) {
@@ -217,14 +242,16 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
         if (!rc)
             rc = launch_sgmv_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, plan, st3, true);
         if (side && cudaEventRecord(side->join, side->s) != cudaSuccess) return LORA_ERR_CUDA;
-        if (!rc) rc = launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank);
+        if (q_side && side && cudaStreamWaitEvent(st, side->join2, 0) != cudaSuccess) return LORA_ERR_CUDA;
+        if (!rc) rc = launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, matrix, tile_ad, v, p->max_rank, f8);
         // no side work is left unjoined, error or not
         if (side && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return LORA_ERR_CUDA;
         if (rc) return rc;
         return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st,
                                   tile_ad);
     }
-    rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st) : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
+    rc = tc ? launch_gemm_tc(p, h_in, h_out, x, W, y, T, st, 0, nullptr, nullptr, 0, f8)
+            : launch_base_gemm(p, h_in, h_out, x, W, y, T, st);
     if (rc) return rc;
     if ((rc = launch_shrink(p, matrix, h_in, x, v, p->max_rank, seg_starts, seg_adapter, S, T, st))) return rc;
     return launch_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, st);

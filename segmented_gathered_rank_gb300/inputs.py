@@ -174,6 +174,19 @@ class Workload:
             return probe_w(self.seed + 1000 * layer + m, mat.h_out, mat.h_in)
         return _store(self.w_dist.draw(_rng(self.seed, _K_W, layer, m), (mat.h_out, mat.h_in)), self.dtype)
 
+    def W_e4m3(self, m: int = 0, layer: int = 0):
+        """The base weight of matrix m as an FP8 base would hold it: e4m3 codes
+        [h_out x h_in] (uint8) of W / s_w and the per-tensor scale s_w =
+        max|W| / 448 (float32).  Input preparation of the caller's side; the
+        codes come from torch's float8_e4m3fn conversion (every value is within
+        +-448 by the choice of s_w)."""
+        import torch
+        w = np.asarray(self.W(m, layer), np.float32)
+        amax = np.float32(np.max(np.abs(w)))
+        s_w = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+        codes = torch.from_numpy(np.ascontiguousarray(w / s_w, np.float32)).to(torch.float8_e4m3fn)
+        return codes.view(torch.uint8).numpy().copy(), float(s_w)
+
     def adapter(self, a: int, m: int = 0, layer: int = 0):
         """(A_T [r x h_in], B [r x h_out]) of adapter ``a`` on matrix ``m``.
 

@@ -43,7 +43,8 @@ EXPORTS = ["lora_pool_create", "lora_pool_destroy", "lora_pool_load", "lora_pool
            "lora_layer_forward_workspace_size", "lora_layer_forward", "lora_get_error", "lora_strerror",
            "lora_launch_count", "lora_layer_forward_noalloc", "lora_tier_cache_create", "lora_tier_cache_destroy",
            "lora_tier_cache_touch", "lora_tier_cache_resident", "lora_tier_sim", "lora_pool_load_async",
-           "lora_pool_unload_async", "lora_pool_prefetch"]
+           "lora_pool_unload_async", "lora_pool_prefetch", "lora_quantize_e4m3",
+           "lora_layer_forward_fp8_workspace_size", "lora_layer_forward_fp8"]
 
 if not os.path.exists(_build.LIB):
     raise ImportError(f"CUDA library {_build.LIB} is not built: run segmented_gathered_rank_gb300.build.build()")
@@ -87,6 +88,9 @@ class AdapterSrc(ctypes.Structure):
 _sig("lora_pool_load_async", _I, _P, _I, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P)
 _sig("lora_pool_unload_async", _I, _P, _I, _I, _P)
 _sig("lora_pool_prefetch", _I, _P, ctypes.POINTER(AdapterSrc), _I, _P)
+_sig("lora_quantize_e4m3", _I, _P, _I, _I, _P, _P, _P)
+_sig("lora_layer_forward_fp8_workspace_size", ctypes.c_size_t, _P, _I, _I, _I)
+_sig("lora_layer_forward_fp8", _I, _P, _I, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _P, ctypes.c_size_t, _P)
 _sig("lora_tier_cache_create", _I, ctypes.POINTER(_P), _I, _I, _I)
 _sig("lora_tier_cache_destroy", _I, _P)
 _sig("lora_tier_cache_touch", _I, _P, _I, ctypes.POINTER(_I))
@@ -277,3 +281,21 @@ def lora_tier_sim(trace, n_keys: int, gpu_slots: int, host_slots: int) -> tuple[
     _check(_lib.lora_tier_sim(ctypes.c_void_p(tr.ctypes.data), len(tr), n_keys, gpu_slots, host_slots, counts),
            "lora_tier_sim")
     return int(counts[0]), int(counts[1]), int(counts[2])
+
+
+def lora_quantize_e4m3(x, T, h, q, sx, stream=None) -> None:
+    """Per-row e4m3 codes (uint8 tensor) and fp32 scales of a bf16 tensor."""
+    _check(_lib.lora_quantize_e4m3(_dptr(x), T, h, _dptr(q), _dptr(sx), _stream(stream)), "lora_quantize_e4m3")
+
+
+def lora_layer_forward_fp8_workspace_size(pool, matrix, S, T) -> int:
+    return int(_lib.lora_layer_forward_fp8_workspace_size(pool, matrix, S, T))
+
+
+def lora_layer_forward_fp8(pool, matrix, x, W8, w_scale, y, seg_starts, seg_adapter, S, T, workspace, ws_bytes=None,
+                           stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.lora_layer_forward_fp8(pool, matrix, _dptr(x), _dptr(W8), float(w_scale), _dptr(y),
+                                       _dptr(seg_starts), _dptr(seg_adapter), S, T, _dptr(workspace), ws_bytes,
+                                       _stream(stream)), "lora_layer_forward_fp8")
