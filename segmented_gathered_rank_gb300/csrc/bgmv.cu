@@ -550,6 +550,312 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Compacted mode, for adapter-id ranges large next to the batch (a pool of
+// thousands of adapters serving a few hundred decode tokens).  The grid no
+// longer has a cluster per id: G persistent clusters (as many as the GPU holds,
+// at most the item bound min(T, n_ids) + T / kTok) walk the batch's items.
+// After the wait on the previous kernel every CTA reads the ids, counts the
+// tokens of each adapter and scans ceil(count / kTok), which numbers the items
+// (adapter, chunk) of the adapters present in the batch; cluster c takes items
+// c, 2G-1-c, 2G+c, ... (snake order).  No page is read for an adapter the batch
+// does not use (measured: 2048 adapters loaded, 256 decode tokens over about
+// 245 of them, 4096 x 4096: 74 us per launch).  Each item runs as in
+// bgmv_cluster_kernel; the exchange
+// barriers' phases run on across items: round R (every 16-rank chunk of every
+// item the cluster takes) completes phase R of bars[0] and, when another
+// round follows, of bars[1].  All CTAs of a cluster derive the same items and
+// ranks from the same ids and table, so they agree on every phase and none
+// signals a peer after its last round.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline size_t bgmv_compact_smem(int slice_in, int slice_out, int T, int n_ids, int rec_ints) {
+    const int pin = slice_in + 8, pout = slice_out + 8;
+    const int a = kJ * pin * 2, red = kWarps * kTok * kJ * 4;
+    return (size_t)(a > red ? a : red) + (size_t)kJ * pout * 2 + (size_t)kTok * pin * 2 + (size_t)kTok * pout * 2 +
+           (size_t)2 * kTok * kVPitch * 2 + (size_t)kC * kTok * kJ * 4 + 16 +
+           (size_t)(rec_ints + kWarps + 2 + kTok + T + n_ids + 1) * 4 + 16;
+}
+
+// collect_tokens with one barrier: warp w scans its contiguous slice of the ids
+// and counts the tokens of adapter a; after the warps' counts are published
+// each warp writes its matches whose rank among all of a's tokens (index order)
+// falls in chunk c.  The same ordered list as collect_tokens.
+__device__ int collect_tokens_sliced(const int *ids, int T, int a, int c, int *tok, int *wcnt) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = (T + kWarps - 1) / kWarps, lo = min(T, warp * per), hi = min(T, lo + per);
+    int n = 0;
+    for (int t0 = lo; t0 < hi; t0 += 32) {
+        const int t = t0 + lane;
+        n += __popc(__ballot_sync(0xffffffffu, t < hi && ids[t] == a));
+    }
+    if (lane == 0) wcnt[warp] = n;
+    __syncthreads();
+    int run = 0, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) run += wcnt[w];
+        total += wcnt[w];
+    }
+    const int first = c * kTok;
+    if (run < first + kTok && run + n > first) {
+        for (int t0 = lo; t0 < hi; t0 += 32) {
+            const int t = t0 + lane;
+            const bool hit = t < hi && ids[t] == a;
+            const unsigned m = __ballot_sync(0xffffffffu, hit);
+            const int pos = run + __popc(m & ((1u << lane) - 1u)) - first;
+            if (hit && pos >= 0 && pos < kTok) tok[pos] = t;
+            run += __popc(m);
+        }
+    }
+    __syncthreads();
+    const int cnt = total - first;
+    return cnt < 0 ? 0 : (cnt > kTok ? kTok : cnt);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) bgmv_compact_kernel(BgmvParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = (int)cluster.block_rank();
+    const int G = gridDim.x / kC, cid = blockIdx.x / kC;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const PoolView &pv = p.pv;
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
+    const int pin = p.slice_in + 8, pout = p.slice_out + 8;
+    const int a_bytes = max(kJ * pin * 2, kWarps * kTok * kJ * 4);
+    __nv_bfloat16 *sA = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [kJ][pin]   rows of A_T
+    float *red = reinterpret_cast<float *>(smem_raw);                    // [kWarps][kTok*kJ] (over sA)
+    __nv_bfloat16 *sB = reinterpret_cast<__nv_bfloat16 *>(smem_raw + a_bytes);   // [kJ][pout] rows of B
+    __nv_bfloat16 *sX = sB + kJ * pout;                                  // [kTok][pin] rows of x
+    __nv_bfloat16 *sY = sX + kTok * pin;                                 // [kTok][pout] rows of y
+    __nv_bfloat16 *sVh = sY + kTok * pout;                               // [kTok][kVPitch] s v, high part
+    __nv_bfloat16 *sVl = sVh + kTok * kVPitch;                           // [kTok][kVPitch] residual
+    float *recv = reinterpret_cast<float *>(sVl + kTok * kVPitch);       // [kC][kTok*kJ] partials of every CTA
+    uint64_t *bars = reinterpret_cast<uint64_t *>(recv + kC * kTok * kJ); // [0] partials in, [1] consumed
+    int *rec = reinterpret_cast<int *>(bars + 2);                        // [rec_ints]
+    int *warp_tot = rec + pv.rec_ints;                                   // [kWarps + 2]
+    int *tok = warp_tot + kWarps + 2;                                    // [kTok]
+    int *sids = tok + kTok;                                              // [T]
+    int *hist = sids + p.T;                                              // [n_ids + 1]
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], kC);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    for (int i = tid; i <= p.n_ids; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+
+    // ---- the batch's items: every CTA numbers them the same way
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    for (int t = tid; t < p.T; t += kThreads) {
+        const int id = p.ids[t];
+        sids[t] = id;
+        if (id >= 0 && id < p.n_ids) atomicAdd(&hist[id], 1);
+        else if (blockIdx.x == 0 && id >= p.n_ids) flag(pv.status, LORA_DEV_BAD_ADAPTER);
+    }
+    __syncthreads();
+    for (int i = tid; i < p.n_ids; i += kThreads) hist[i] = (hist[i] + kTok - 1) / kTok;
+    __syncthreads();
+    const int n_items = block_exclusive_scan(hist, p.n_ids, warp_tot);
+    auto item_at = [&](int k) { return k * G + ((k & 1) ? G - 1 - cid : cid); };
+    auto adapter_of_item = [&](int i) {   // last adapter whose first item index is <= i
+        int lo = 0, hi = p.n_ids - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (hist[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+    auto rank_in_table = [&](int a) {
+        return pv.table[((long long)a * pv.n_matrices + p.m) * pv.rec_ints];
+    };
+    int total_rounds = 0;
+    for (int k = 0;; ++k) {
+        const int i = item_at(k);
+        if (i >= n_items) break;
+        const int r = min(max(rank_in_table(adapter_of_item(i)), 0), pv.max_rank);
+        total_rounds += (r + kJ - 1) / kJ;
+    }
+
+    const int k0 = crank * p.slice_in;
+    const int nkv = max(0, min(p.slice_in, p.h_in - k0)) / 8;
+    const int n0 = crank * p.slice_out;
+    const int ncv = max(0, min(p.slice_out, p.h_out - n0)) / 8;
+    const int kvpow = 31 - __clz(max(p.slice_in / 8, 1));
+    const int cvpow = 31 - __clz(max(p.slice_out / 8, 1));
+    const int g = lane >> 2, q = lane & 3;
+    const int cw = p.slice_out / kWarps;
+    const int wc0 = warp * cw;
+    const int ntiles = cw / 8;
+    int R = 0;
+
+    for (int k = 0;; ++k) {
+        const int ii = item_at(k);
+        if (ii >= n_items) break;
+        const int a = adapter_of_item(ii), c = ii - hist[a];
+        __syncthreads();                        // the previous item's readers of rec, tok and the tiles are done
+        for (int i = tid; i < pv.rec_ints; i += kThreads)
+            rec[i] = pv.table[((long long)a * pv.n_matrices + p.m) * pv.rec_ints + i];
+        const int ntok = collect_tokens_sliced(sids, p.T, a, c, tok, warp_tot);   // ends with a barrier
+        const int rank = min(max(rec[0], 0), pv.max_rank);
+        if (rec[0] < 0) {
+            if (crank == 0 && tid == 0) flag(pv.status, LORA_DEV_BAD_ADAPTER);
+            continue;
+        }
+        const int n_jc = (rank + kJ - 1) / kJ;
+        if (n_jc == 0) continue;               // rank 0: y stays as it is (counted as no round above)
+        const float scale = __int_as_float(rec[1]);
+        auto prefetch_pages = [&](int jc) {
+            const int jn = min(kJ, rank - jc * kJ);
+            const int sv_in = p.slice_in / 8, sv_out = p.slice_out / 8;
+            for (int i = tid; i < kJ * sv_in; i += kThreads) {
+                const int jj = i >> kvpow, kv = i & (sv_in - 1);
+                __nv_bfloat16 *dst = sA + jj * pin + kv * 8;
+                if (jj < jn && kv < nkv)
+                    cp_async16(dst, page_row<__nv_bfloat16>(pv, clamp_page(pv, rec[kRecHeader + jc * kJ + jj])) + k0 +
+                                        kv * 8);
+                else
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+            }
+            for (int i = tid; i < kJ * sv_out; i += kThreads) {
+                const int jj = i >> cvpow, cv = i & (sv_out - 1);
+                __nv_bfloat16 *dst = sB + jj * pout + cv * 8;
+                if (jj < jn && cv < ncv)
+                    cp_async16(dst, page_row<__nv_bfloat16>(pv, clamp_page(pv, rec[kRecHeader + rank + jc * kJ + jj])) +
+                                        n0 + cv * 8);
+                else
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+            }
+        };
+        prefetch_pages(0);
+        {
+            const int sv_in = p.slice_in / 8, sv_out = p.slice_out / 8;
+            for (int i = tid; i < kTok * sv_in; i += kThreads) {
+                const int tl = i >> kvpow, kv = i & (sv_in - 1);
+                __nv_bfloat16 *dst = sX + tl * pin + kv * 8;
+                if (tl < ntok && kv < nkv)
+                    cp_async16(dst, p.x + (long long)tok[tl] * p.h_in + k0 + kv * 8);
+                else
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+            }
+            for (int i = tid; i < ntok * sv_out; i += kThreads) {
+                const int tl = i >> cvpow, cv = i & (sv_out - 1);
+                if (cv < ncv) cp_async16(sY + tl * pout + cv * 8, p.y + (long long)tok[tl] * p.h_out + n0 + cv * 8);
+            }
+        }
+        float dacc[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dacc[t][e] = 0.f;
+        for (int jc = 0; jc < n_jc; ++jc, ++R) {
+            const int jn = min(kJ, rank - jc * kJ);
+            if (jc > 0) prefetch_pages(jc);
+            cp_async_wait_all();
+            __syncthreads();
+            {
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                const int ksteps = p.slice_in / 16;
+                for (int ks = warp; ks < ksteps; ks += kWarps) {
+                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                    ldsm_x4(sX + (lane & 15) * pin + ks * 16 + (lane >> 4) * 8, a0, a1, a2, a3);
+                    ldsm_x4(sA + ((lane & 7) + ((lane >> 4) << 3)) * pin + ks * 16 + ((lane >> 3) & 1) * 8, b0, b1,
+                            b2, b3);
+                    mma16816(d0, a0, a1, a2, a3, b0, b1);
+                    mma16816(d1, a0, a1, a2, a3, b2, b3);
+                }
+                __syncthreads();     // every warp is done with sA: the partials overwrite it
+                float *rw = red + warp * kTok * kJ;
+                rw[g * kJ + 2 * q] = d0[0];
+                rw[g * kJ + 2 * q + 1] = d0[1];
+                rw[(g + 8) * kJ + 2 * q] = d0[2];
+                rw[(g + 8) * kJ + 2 * q + 1] = d0[3];
+                rw[g * kJ + 8 + 2 * q] = d1[0];
+                rw[g * kJ + 8 + 2 * q + 1] = d1[1];
+                rw[(g + 8) * kJ + 8 + 2 * q] = d1[2];
+                rw[(g + 8) * kJ + 8 + 2 * q + 1] = d1[3];
+            }
+            __syncthreads();
+            bool failed = false;
+            {
+                float part = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) part += red[w * kTok * kJ + tid];   // kThreads == kTok * kJ
+                if (R == 0) asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");   // peers' barriers exist
+                if (R > 0 && !wait_bar(&bars[1], (uint32_t)(R - 1) & 1u)) failed = true;
+                if (!failed) {
+#pragma unroll
+                    for (int r = 0; r < kC; ++r) store_async_remote(recv + crank * kTok * kJ + tid, part, &bars[0], r);
+                }
+                if (tid == 0) mbar_arrive_expect_tx(&bars[0], (uint32_t)(kC * kTok * kJ * sizeof(float)));
+            }
+            if (!failed && !wait_bar(&bars[0], (uint32_t)R & 1u)) failed = true;
+            if (__syncthreads_or(failed)) {
+                // a second bounded window for peers' late partials before the CTA leaves
+                if (tid == 0) flag(pv.status, LORA_DEV_WAIT_TIMEOUT);
+                wait_bar(&bars[0], (uint32_t)R & 1u);
+                cp_async_wait_all();
+                return;
+            }
+            {
+                float sum = 0.f;
+#pragma unroll
+                for (int r = 0; r < kC; ++r) sum += recv[r * kTok * kJ + tid];
+                const int tl = tid >> 4, jj = tid & 15;
+                const float val = jj < jn ? scale * sum : 0.f;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+                sVh[tl * kVPitch + jj] = hi;
+                sVl[tl * kVPitch + jj] = __float2bfloat16_rn(val - __bfloat162float(hi));
+            }
+            __syncthreads();     // receive slots read; sA and sB may be refilled
+            if (tid == 0 && R + 1 < total_rounds)
+                for (int r = 0; r < kC; ++r) remote_arrive(&bars[1], r);
+            {
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                ldsm_x4(sVh + (lane & 15) * kVPitch + (lane >> 4) * 8, h0, h1, h2, h3);
+                ldsm_x4(sVl + (lane & 15) * kVPitch + (lane >> 4) * 8, l0, l1, l2, l3);
+#pragma unroll
+                for (int t = 0; t < 8; t += 2) {
+                    if (t >= ntiles) break;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(sB + ((lane & 7) + ((lane >> 3) & 1) * 8) * pout + wc0 + (t + (lane >> 4)) * 8, b0, b1,
+                              b2, b3);
+                    mma16816(dacc[t], h0, h1, h2, h3, b0, b1);
+                    mma16816(dacc[t], l0, l1, l2, l3, b0, b1);
+                    mma16816(dacc[t + 1], h0, h1, h2, h3, b2, b3);
+                    mma16816(dacc[t + 1], l0, l1, l2, l3, b2, b3);
+                }
+            }
+            __syncthreads();
+        }
+        // y += delta in the shared y tile, then coalesced stores
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (t >= ntiles) break;
+            const int col = wc0 + t * 8 + 2 * q;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                __nv_bfloat162 *yy = reinterpret_cast<__nv_bfloat162 *>(sY + (g + 8 * h) * pout + col);
+                const float2 f = __bfloat1622float2(*yy);
+                *yy = __floats2bfloat162_rn(f.x + dacc[t][2 * h], f.y + dacc[t][2 * h + 1]);
+            }
+        }
+        __syncthreads();
+        {
+            const int sv_out = p.slice_out / 8;
+            for (int i = tid; i < ntok * sv_out; i += kThreads) {
+                const int tl = i >> cvpow, cv = i & (sv_out - 1);
+                if (cv < ncv)
+                    *reinterpret_cast<uint4 *>(p.y + (long long)tok[tl] * p.h_out + n0 + cv * 8) =
+                        *reinterpret_cast<const uint4 *>(sY + tl * pout + cv * 8);
+            }
+        }
+    }
+    if (R == 0) asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+    cp_async_wait_all();
+}
+
 int pow2_at_least(int v) {
     int p = 1;
     while (p < v) p <<= 1;
@@ -563,14 +869,24 @@ int pow2_at_least(int v) {
 static int slice_in_of(int h_in) { return pow2_at_least(std::max(16, (h_in + kC - 1) / kC)); }
 static int slice_out_of(int h_out) { return pow2_at_least(std::max(128, (h_out + kC - 1) / kC)); }
 
-// Whether the clustered kernel takes this problem (else the per-token kernel does).
+// Whether the clustered kernels take this problem (else the per-token kernel
+// does): bf16, a batch of at most kMaxT tokens, and an id range the compacted
+// mode's histogram holds.  (Measured: for a 16384-token batch of 128-token
+// runs over 1024 mixed-rank adapters, 768 wide, consecutive kMaxT-token chunks
+// of the compacted kernel took 412 us per call and the per-token kernel 103
+// us, so larger batches stay on the per-token kernel.)
+constexpr int kMaxCompactIds = 8192;
 bool bgmv_cluster_ok(const lora_pool *pool, int h_in, int h_out, int T, int n_ids) {
-    return pool->dtype == LORA_BF16 && T <= kMaxT && n_ids <= kMaxIds && n_ids > 0 && h_in % 16 == 0 &&
+    return pool->dtype == LORA_BF16 && T <= kMaxT && n_ids > 0 && n_ids <= kMaxCompactIds && h_in % 16 == 0 &&
            slice_in_of(h_in) <= kMaxSliceIn && slice_out_of(h_out) <= kMaxSliceOut;
 }
 
-int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, const void *x, void *y,
-                        const int *token_adapter, int T, int n_ids, cudaStream_t st) {
+// A batch of at most kMaxT tokens.  Id-indexed mode (a cluster per adapter id,
+// pages prefetched before the wait on the previous kernel) while the id range is
+// small next to the batch; compacted persistent mode otherwise, so the grid and
+// the page reads follow the batch, not the id range.
+static int launch_bgmv_chunk(const lora_pool *pool, int matrix, int h_in, int h_out, const __nv_bfloat16 *x,
+                             __nv_bfloat16 *y, const int *ids, int T, int n_ids, cudaStream_t st) {
     BgmvParams p;
     p.pv = pool->view();
     p.m = matrix;
@@ -580,19 +896,12 @@ int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, 
     p.slice_out = slice_out_of(h_out);
     p.n_ids = n_ids;
     p.T = T;
-    p.x = static_cast<const __nv_bfloat16 *>(x);
-    p.y = static_cast<__nv_bfloat16 *>(y);
-    p.ids = token_adapter;
-    const BgmvLayout lay = bgmv_layout(p.slice_in, p.slice_out, T, n_ids);
-    const size_t smem = (size_t)lay.a_bytes + (size_t)kJ * (p.slice_out + 8) * 2 + (size_t)lay.xy_bytes +
-                        (size_t)2 * kTok * kVPitch * 2 + (size_t)kC * kTok * kJ * 4 + 16 +
-                        (size_t)(p.pv.rec_ints + kWarps + 2) * 4 + sizeof(Item) + 16;
-    if (smem_optin(reinterpret_cast<const void *>(bgmv_cluster_kernel), smem)) return LORA_ERR_CUDA;
-    const int items = n_ids + (T + kTok - 1) / kTok;
+    p.x = x;
+    p.y = y;
+    p.ids = ids;
+    const bool compact = n_ids > std::max(64, T / 8) || n_ids > kMaxIds;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(items * kC);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -603,9 +912,39 @@ int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, bgmv_cluster_kernel, p);
+    cudaError_t e;
+    if (!compact) {
+        const BgmvLayout lay = bgmv_layout(p.slice_in, p.slice_out, T, n_ids);
+        const size_t smem = (size_t)lay.a_bytes + (size_t)kJ * (p.slice_out + 8) * 2 + (size_t)lay.xy_bytes +
+                            (size_t)2 * kTok * kVPitch * 2 + (size_t)kC * kTok * kJ * 4 + 16 +
+                            (size_t)(p.pv.rec_ints + kWarps + 2) * 4 + sizeof(Item) + 16;
+        if (smem_optin(reinterpret_cast<const void *>(bgmv_cluster_kernel), smem)) return LORA_ERR_CUDA;
+        cfg.gridDim = dim3((n_ids + (T + kTok - 1) / kTok) * kC);
+        cfg.dynamicSmemBytes = smem;
+        e = cudaLaunchKernelEx(&cfg, bgmv_cluster_kernel, p);
+    } else {
+        const size_t smem = bgmv_compact_smem(p.slice_in, p.slice_out, T, n_ids, p.pv.rec_ints);
+        if (smem_optin(reinterpret_cast<const void *>(bgmv_compact_kernel), smem)) return LORA_ERR_CUDA;
+        cfg.dynamicSmemBytes = smem;
+        cfg.gridDim = dim3(kC);
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, bgmv_compact_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            active = 0;
+        }
+        const int bound = std::min(T, n_ids) + (T + kTok - 1) / kTok;
+        const int clusters = std::max(1, std::min(bound, active > 0 ? active : num_sms() / kC));
+        cfg.gridDim = dim3(clusters * kC);
+        e = cudaLaunchKernelEx(&cfg, bgmv_compact_kernel, p);
+    }
     count_launch();
     return cuda_status(e);
+}
+
+int launch_bgmv_cluster(const lora_pool *pool, int matrix, int h_in, int h_out, const void *x, void *y,
+                        const int *token_adapter, int T, int n_ids, cudaStream_t st) {
+    return launch_bgmv_chunk(pool, matrix, h_in, h_out, static_cast<const __nv_bfloat16 *>(x),
+                             static_cast<__nv_bfloat16 *>(y), token_adapter, T, n_ids, st);
 }
 
 }  // namespace lora

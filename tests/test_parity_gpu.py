@@ -568,3 +568,47 @@ def test_rank0_and_zero_b_decode_layer():
     assert np.array_equal(yd[keep], np.zeros_like(yd[keep]))
     ydr, st = oracle_delta(w, 0, None)
     assert st == 0 and rel_err(yd, ydr) <= TOL_Y[w.dtype]
+
+
+# ---------------------------------------------------------------------------
+# BGMV launch modes.  The grid follows the batch: a pool whose adapter-id range
+# is large next to the batch runs the compacted mode (persistent clusters over
+# the items of the adapters present); batches above the clustered kernels'
+# limit run on the per-token kernel.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [256, 2048])      # compacted mode; its largest batch
+def test_bgmv_2048_adapter_pool(T):
+    ranks = np.tile(np.array([16, 8, 32, 16], np.int32), 512)             # 2048 adapters
+    w = I.random_case(111, T=T, decode=True, ranks=ranks, h_in=1024, h_out=1024)
+    used = set(w.used_adapters().tolist())
+    assert len(used) > 200
+    with H.DevicePool(w, matrices=[0], filler=lambda a: a not in used) as dp:
+        tok = H.int_tensor(w.token_adapter)
+        x = H.to_device(w.x(0), w.dtype)
+        y0 = w.y0(0)
+        y = H.to_device(y0, w.dtype)
+        L.lora_bgmv(dp.handle, 0, x, y, tok, w.T)
+        word = dp.check_device_status()
+    assert word == 0
+    yr, st = oracle_delta(w, 0, y0)
+    assert st == 0 and rel_err(H.to_host(y), yr) <= TOL_Y[w.dtype]
+
+
+@pytest.mark.parametrize("n_adapters", [40, 600])
+def test_bgmv_batch_above_the_clustered_limit(n_adapters):
+    ranks = np.tile(np.array([16, 64, 8, 0, 32], np.int32), n_adapters // 5)
+    w = I.random_case(112 + n_adapters, T=5000, decode=True, ranks=ranks, h_in=512, h_out=256)
+    w.token_adapter[::13] = -1
+    w.seg_adapter = w.token_adapter.copy()
+    check_bgmv(w)
+
+
+@pytest.mark.parametrize("dtype", [I.BF16])
+def test_bgmv_compacted_integer_probe_bitexact(dtype):
+    ranks = np.tile(np.array([4, 8, 16, 2], np.int32), 50)               # 200 ids for 64 tokens
+    w = I.integer_probe(seed=113, T=64, lengths=[1] * 64, h_in=256, h_out=128, ranks=ranks, dtype=dtype)
+    w.token_adapter = np.repeat(w.seg_adapter, np.diff(w.seg_starts)).astype(np.int32)
+    y, y0, word = run_bgmv(w)
+    assert word == 0
+    yr, _ = oracle_delta(w, 0, y0)
+    assert _exact(yr) and np.array_equal(y, yr)
