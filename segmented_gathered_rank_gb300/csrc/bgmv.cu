@@ -486,7 +486,12 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_cluster_kernel(BgmvParams p)
         }
         if (!failed && !wait_bar(&bars[0], (uint32_t)jc & 1u)) failed = true;
         if (__syncthreads_or(failed)) {
+            // Leaving while a peer could still store its partial here would let
+            // that store land in a finished CTA: give this round's partials a
+            // second bounded window first (a peer that gave up itself sends no
+            // more; one that is only late lands within it).
             if (tid == 0) flag(pv.status, LORA_DEV_WAIT_TIMEOUT);
+            wait_bar(&bars[0], (uint32_t)jc & 1u);
             cp_async_wait_all();
             return;
         }
