@@ -275,17 +275,14 @@ struct PlanParams {
     Unit *su, *eu;      // with units: shrink and expand units of the work items (counts plan[2], plan[3])
     int npc_s;          // ranks per shrink unit
     int nb_total;       // column blocks of kNb in h_out
-    int bpu;            // column blocks per expand unit of cheap items
+    int e_ctas;         // resident CTAs of the expand-units kernel
     int rank_cap;       // ranks beyond this are not computed (the v row length)
     int body;           // ints of the counting-sort area of shared memory
 };
 
-// Column blocks per expand unit from an item's cost per block: its y rows,
-// read and written once per pass of up to 32 ranks, plus its B rows.
-__device__ __forceinline__ int expand_bpu(int nt, int r, int bpu_cheap) {
-    const int cost = 2 * nt * ((r + 31) / 32) + r;
-    return cost >= 48 ? 1 : (cost >= 24 ? 2 : bpu_cheap);
-}
+// An item's expand cost per column block, in 256-byte rows: its y rows, read
+// and written once per pass of up to 32 ranks, plus its B rows.
+__device__ __forceinline__ int expand_cost(int nt, int r) { return 2 * nt * ((r + 31) / 32) + r; }
 
 __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     extern __shared__ __align__(16) int sm[];
@@ -436,11 +433,8 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
                     const unsigned left = ~(unsigned)w.pad & all;
                     const int nh = ((left & 0xffffu) != 0u) + ((left >> 16) != 0u);
                     const int nch = (r + p.npc_s - 1) / p.npc_s;
-                    const int bpu = expand_bpu(w.nt, r, p.bpu);
-                    const int ne = (p.nb_total + bpu - 1) / bpu;
                     const bool costly_s = min(w.nt, kRowsS) + min(r, p.npc_s) >= 32;
-                    c = make_int4(costly_s ? nh * nch : 0, costly_s ? 0 : nh * nch, bpu == 1 ? ne : 0,
-                                  bpu == 1 ? 0 : ne);
+                    c = make_int4(costly_s ? nh * nch : 0, costly_s ? 0 : nh * nch, 0, 0);   // expand: below
                 }
                 sitem[k] = make_int4(w.a, w.off, w.nt, w.pad);
                 ucnt[k] = c;
@@ -452,9 +446,45 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
     const int n_work = *wcount;
     if (tid == 0) p.plan[1] = n_work;
     if (!p.su) return;
+    // Expand units: column-block ranges sized so that the units of the whole
+    // batch fill the expand kernel's resident CTAs about once (each unit pays a
+    // few dependent global round trips before its copies start, so many small
+    // units cost more than the data they move).  Item k gets
+    // max(1, floor(C_k / target)) units, C_k its cost over all column blocks and
+    // target the batch's total cost per CTA; units whose cost reaches the target
+    // are listed first.  Integer sums keep the choice deterministic.
+    {
+        unsigned long long part = 0;
+        for (int k = tid; k < n_work; k += kPlanThreads)
+            if (srank[k] > 0) part += (unsigned long long)p.nb_total * expand_cost(sitem[k].z, srank[k]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        unsigned long long *wsum = reinterpret_cast<unsigned long long *>(wtot4);
+        if (lane == 0) wsum[warp] = part;
+        __syncthreads();
+        unsigned long long total = 0;
+#pragma unroll
+        for (int w = 0; w < nwarps; ++w) total += wsum[w];
+        const unsigned long long target = max(1ull, total / (unsigned long long)max(1, p.e_ctas));
+        for (int k = tid; k < n_work; k += kPlanThreads) {
+            const int r = srank[k];
+            if (r <= 0) continue;
+            const int cost = expand_cost(sitem[k].z, r);
+            const unsigned long long ck = (unsigned long long)p.nb_total * cost;
+            const int units = (int)max(1ull, min((unsigned long long)p.nb_total, ck / target));
+            const int bpu = min(kMaxBlocksPerUnit, (p.nb_total + units - 1) / units);
+            const int ne = (p.nb_total + bpu - 1) / bpu;
+            const bool costly = (unsigned long long)bpu * cost >= target;
+            ucnt[k].z = costly ? ne : 0;
+            ucnt[k].w = costly ? 0 : ne;
+            srank[k] = r | (costly ? 1 << 12 : 0) | (bpu << 16);     // r <= 1024
+        }
+        __syncthreads();                 // wsum (over the scan's scratch) is read; the counts are written
+    }
     const int4 tot = block_scan4<kPlanThreads>(ucnt, n_work, wtot4);
     for (int k = tid; k < n_work; k += kPlanThreads) {
-        const int r = srank[k];
+        const int r = srank[k] & 0xfff, bpu = srank[k] >> 16;
+        const bool costly = (srank[k] >> 12) & 1;
         if (r <= 0) continue;
         const int4 w = sitem[k], c = ucnt[k];
         const unsigned all = w.z >= 32 ? 0xffffffffu : ((1u << w.z) - 1u);
@@ -466,8 +496,7 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
             if (!((left >> (16 * h)) & 0xffffu)) continue;
             for (int ch = 0; ch < nch; ++ch) p.su[u++] = Unit{w.x, w.y, w.z | (h << 6) | (ch << 8), w.w};
         }
-        const int bpu = expand_bpu(w.z, r, p.bpu);
-        u = bpu == 1 ? c.z : tot.z + c.w;
+        u = costly ? c.z : tot.z + c.w;
         for (int b = 0; b < p.nb_total; b += bpu)
             p.eu[u++] = Unit{w.x, w.y, w.z | (min(bpu, p.nb_total - b) << 6) | (b << 10), w.w};
     }
@@ -1246,6 +1275,21 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_units_kernel(ExpandP
     }
 }
 
+// The units kernel's ranks per pass, shared memory and grid (one CTA per
+// resident slot: the SMs times the CTAs one SM holds); grid 0 on error.
+int expand_units_kpc(const lora_pool *pool) { return std::min(32, (pool->max_rank + 15) / 16 * 16); }
+size_t expand_units_smem(const lora_pool *pool) {
+    const int kpc = expand_units_kpc(pool);
+    return (size_t)kStagesE * (kM + kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (kpc + 8) * 2 +
+           (size_t)(kM + 8 + pool->view().rec_ints) * 4 + 16;
+}
+int expand_units_grid(const lora_pool *pool) {
+    int occ = 0;
+    if (smem_optin(reinterpret_cast<const void *>(sgmv_expand_units_kernel), expand_units_smem(pool), kThreadsE, &occ))
+        return 0;
+    return num_sms() * std::max(1, occ);
+}
+
 // Upper bound on items: every non-empty segment (or adapter) has at least
 // one chunk, and the chunks together cover T tokens.
 int item_bound(int groups, int T) { return std::min(groups, T) + (T + kM - 1) / kM; }
@@ -1329,7 +1373,8 @@ int launch_sgmv_plan(const lora_pool *pool, int matrix, const int *seg_starts, c
     p.eu = units ? reinterpret_cast<Unit *>(plan + L.eu) : nullptr;
     p.npc_s = shrink_npc(pool);
     p.nb_total = (std::max(0, pool->mat_h_out[matrix]) + kNb - 1) / kNb;
-    p.bpu = 8;
+    p.e_ctas = units ? expand_units_grid(pool) : 1;
+    if (units && p.e_ctas <= 0) return LORA_ERR_CUDA;
     p.rank_cap = pool->max_rank;
     const size_t smem = plan_smem(pool, matrix, S, T, units, &p.body);
     if (smem_optin(reinterpret_cast<const void *>(sgmv_plan_kernel), smem)) return LORA_ERR_CUDA;
@@ -1431,13 +1476,10 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
         // layer plan: persistent CTAs over the plan's expand units, in passes of at most 32
         // ranks (a third CTA per SM; only units of ranks above 32 take more passes)
         p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).eu);
-        p.kpc = std::min(32, p.kpc);
-        const size_t smem_u = (size_t)kStagesE * (kM + p.kpc) * (kNb + 8) * 2 + (size_t)2 * kM * (p.kpc + 8) * 2 +
-                              (size_t)(kM + 8 + p.pv.rec_ints) * 4 + 16;
-        int occ = 0;
-        if (smem_optin(reinterpret_cast<const void *>(sgmv_expand_units_kernel), smem_u, kThreadsE, &occ))
-            return LORA_ERR_CUDA;
-        sgmv_expand_units_kernel<<<num_sms() * std::max(1, occ), kThreadsE, smem_u, st>>>(p);
+        p.kpc = expand_units_kpc(pool);
+        const int grid = expand_units_grid(pool);
+        if (grid <= 0) return LORA_ERR_CUDA;
+        sgmv_expand_units_kernel<<<grid, kThreadsE, expand_units_smem(pool), st>>>(p);
         count_launch();
         return cuda_status(cudaGetLastError());
     }
