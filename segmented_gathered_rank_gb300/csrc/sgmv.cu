@@ -472,7 +472,11 @@ __global__ void __launch_bounds__(kPlanThreads) sgmv_plan_kernel(PlanParams p) {
             const int cost = expand_cost(sitem[k].z, r);
             const unsigned long long ck = (unsigned long long)p.nb_total * cost;
             const int units = (int)max(1ull, min((unsigned long long)p.nb_total, ck / target));
-            const int bpu = min(kMaxBlocksPerUnit, (p.nb_total + units - 1) / units);
+            const int passes = (r + 31) / 32;
+            // an item of 2..kStagesE rank passes takes single-block units, so that
+            // every one of its rows gets the single rounding of y of that path,
+            // whichever item the row falls in (the grouping follows atomics)
+            const int bpu = passes > 1 && passes <= kStagesE ? 1 : min(kMaxBlocksPerUnit, (p.nb_total + units - 1) / units);
             const int ne = (p.nb_total + bpu - 1) / bpu;
             const bool costly = (unsigned long long)bpu * cost >= target;
             ucnt[k].z = costly ? ne : 0;
