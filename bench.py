@@ -520,7 +520,8 @@ class FusedLayer(Runner):
     @staticmethod
     def describe(layers: int = 32) -> str:
         return ("fused_layer: 4x1024 prefill + 512 decode tokens, Llama-3-8B q/k/v/o (4096->4096/1024/1024/4096), "
-                "128 adapters Zipf(1.0), rank 16 (adapter 0 rank 128), bf16; step = lora_layer_forward on q,k,v,o")
+                "128 adapters Zipf(1.0), rank 16 (adapter 0 rank 128), bf16; step = lora_layer_forward on q,k,v,o, "
+                "the four independent projections issued on four streams, each with its own workspace")
 
     def __init__(self, seed: int = 0):
         import torch
@@ -535,11 +536,12 @@ class FusedLayer(Runner):
         self.W = [H.to_device(w.W(m), w.dtype) for m in range(4)]
         self.y = [torch.empty((w.T, mt.h_out), dtype=torch.bfloat16, device="cuda") for mt in w.matrices]
         self.ws_bytes = max(L.lora_layer_forward_workspace_size(self.pool.handle, m, w.S, w.T) for m in range(4))
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self._streams(torch)
         self.units_per_step = self.T * 4
         tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
         self.flops = [A.layer_flops(tok, w.ranks, mt.h_in, mt.h_out) for mt in w.matrices]
-        self.dominant = dict(name="lora_layer_forward (base GEMM + adapter term)", bound="tensor",
+        self.dominant = dict(name="lora_layer_forward (base GEMM + adapter term); the four calls of a step run "
+                                  "concurrently, so the time per call is the step's time / 4", bound="tensor",
                              work_per_launch=sum(self.flops) / 4, launches_per_step=4, unit="TFLOP/s")
         self.config = {"workload": self.describe(),
                        "tokens": self.T, "flops_per_step": int(sum(self.flops)),
@@ -548,11 +550,29 @@ class FusedLayer(Runner):
     def _x(self, m):
         return self.x[0] if m < 3 else self.x[3]
 
+    def _streams(self, torch):
+        # q, k, v and o read x (or x_o) and write their own y: each goes on a stream
+        # of its own with a workspace of its own, forked from and joined back to
+        # the step's stream, so one call's latency-bound phases overlap another's GEMM
+        self.wss = [torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda") for _ in range(4)]
+        self.streams = [torch.cuda.Stream() for _ in range(4)]
+        self.fork = torch.cuda.Event()
+        self.done = [torch.cuda.Event() for _ in range(4)]
+
+    def _call(self, m, stream):
+        w = self.w
+        self.L.lora_layer_forward(self.pool.handle, m, self._x(m), self.W[m], self.y[m], self.ss, self.sa, w.S, w.T,
+                                  self.wss[m], self.ws_bytes, stream)
+
     def step(self, stream=None):
-        w, L = self.w, self.L
+        cur = stream if stream is not None else self.torch.cuda.current_stream()
+        self.fork.record(cur)
         for m in range(4):
-            L.lora_layer_forward(self.pool.handle, m, self._x(m), self.W[m], self.y[m], self.ss, self.sa, w.S, w.T,
-                                 self.ws, self.ws_bytes, stream)
+            self.streams[m].wait_event(self.fork)
+            self._call(m, self.streams[m])
+            self.done[m].record(self.streams[m])
+        for m in range(4):
+            cur.wait_event(self.done[m])
 
     def e2e_setup(self):
         self.x_h = {k: v.cpu().pin_memory() for k, v in self.x.items()}
@@ -600,7 +620,7 @@ class FusedLayerFp8(FusedLayer):
     @staticmethod
     def describe(layers: int = 32) -> str:
         return ("fused_layer_fp8: as fused_layer, base weights e4m3 (per-tensor scale), x quantised per row to "
-                "e4m3 inside the call, adapters bf16; step = lora_layer_forward_fp8 on q,k,v,o")
+                "e4m3 inside the call, adapters bf16; step = lora_layer_forward_fp8 on q,k,v,o, on four streams")
 
     def __init__(self, seed: int = 0):
         super().__init__(seed)
@@ -612,16 +632,15 @@ class FusedLayerFp8(FusedLayer):
             self.s_w.append(s_w)
         self.W = None
         self.ws_bytes = max(L.lora_layer_forward_fp8_workspace_size(self.pool.handle, m, w.S, w.T) for m in range(4))
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self._streams(torch)
         self.dominant = dict(self.dominant, name="lora_layer_forward_fp8 (quantise x + FP8 base GEMM + adapter term)",
                              peak_key="fp8")
         self.config = dict(self.config, workload=self.describe())
 
-    def step(self, stream=None):
-        w, L = self.w, self.L
-        for m in range(4):
-            L.lora_layer_forward_fp8(self.pool.handle, m, self._x(m), self.W8[m], self.s_w[m], self.y[m], self.ss,
-                                     self.sa, w.S, w.T, self.ws, self.ws_bytes, stream)
+    def _call(self, m, stream):
+        w = self.w
+        self.L.lora_layer_forward_fp8(self.pool.handle, m, self._x(m), self.W8[m], self.s_w[m], self.y[m], self.ss,
+                                      self.sa, w.S, w.T, self.wss[m], self.ws_bytes, stream)
 
     def cpu_sample(self, budget_s: float):
         import oracle
