@@ -144,33 +144,43 @@ StageLayout stage_layout(const lora_pool *p, int rank) {
 }  // namespace lora
 
 namespace lora {
-// A second stream, per host thread and device, for the part of a layer call
-// that may run beside the main stream's kernels, with the events that fork it
-// from the main stream and join it back.  Under stream capture the fork and
-// join become graph edges.
+// Streams for the parts of a layer call that may run beside the caller's
+// stream, with the events that fork them from it and join them back.  One set
+// per host thread, device and caller stream (up to kSideSets caller streams per
+// thread and device; further ones share the last set made), so that calls issued
+// at once on different streams do not queue behind one another's side work.
+// Under stream capture the forks and joins become graph edges.
 struct SideStream {
     int device = -1;
+    cudaStream_t caller = nullptr;
     cudaStream_t s = nullptr, s2 = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
 };
+constexpr int kSideSets = 16;
 
-static SideStream *side_stream() {
-    thread_local SideStream ss;
+static SideStream *side_stream(cudaStream_t caller) {
+    thread_local SideStream sets[kSideSets];
+    thread_local int used = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (ss.device != dev) {
-        // a stream of another device stays as it is: work of this thread may still use it
-        SideStream n;
-        if (cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&n.s2, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&n.join2, cudaEventDisableTiming) != cudaSuccess)
-            return nullptr;
-        n.device = dev;
-        ss = n;
+    SideStream *last = nullptr;
+    for (int i = 0; i < used; ++i) {
+        if (sets[i].device != dev) continue;
+        if (sets[i].caller == caller) return &sets[i];
+        last = &sets[i];
     }
-    return &ss;
+    if (used == kSideSets) return last;
+    SideStream n;
+    if (cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&n.s2, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.join2, cudaEventDisableTiming) != cudaSuccess)
+        return last;
+    n.device = dev;
+    n.caller = caller;
+    sets[used] = n;
+    return &sets[used++];
 }
 
 // The adapted layer given scratch for v (T x max_rank fp32): base product for
@@ -216,7 +226,7 @@ int layer_forward_impl(const lora_pool *p, int matrix, int h_in, int h_out, cons
             return launch_sgmv_expand(p, matrix, h_out, v, p->max_rank, y, seg_starts, seg_adapter, S, T, plan, st);
         }
         int *tile_ad = sgmv_plan_tiles(p, matrix, T, plan);
-        SideStream *side = side_stream();
+        SideStream *side = side_stream(st);
         cudaStream_t st3 = st;
         if (side && cudaEventRecord(side->fork, st) != cudaSuccess) return LORA_ERR_CUDA;
         if (q_side) {   // FP8: x quantised on the second side stream, joined before the GEMM
