@@ -170,9 +170,17 @@ static SideStream *side_stream(cudaStream_t caller) {
         last = &sets[i];
     }
     if (used == kSideSets) return last;
+    // the side streams take the device's highest priority: their kernels are short
+    // and the caller's stream waits for them, so when an SM frees up their CTAs
+    // should go before the waiting CTAs of long kernels (another call's GEMM)
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) {
+        cudaGetLastError();
+        greatest = 0;
+    }
     SideStream n;
-    if (cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&n.s2, cudaStreamNonBlocking) != cudaSuccess ||
+    if (cudaStreamCreateWithPriority(&n.s, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&n.s2, cudaStreamNonBlocking, greatest) != cudaSuccess ||
         cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&n.join2, cudaEventDisableTiming) != cudaSuccess)
