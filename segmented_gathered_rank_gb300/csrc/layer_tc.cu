@@ -2,8 +2,9 @@
 //
 //   y[t][n] = sum_k x[t][k] W[n][k]
 //
-// "The base part is one big shared matmul for the whole batch"
-// ("Multi-LoRA Serving", section "The kernel trick: gather, do not merge").
+// The base term is computed once for the whole mixed batch, as a single
+// matmul shared by every request ("Multi-LoRA Serving", section "The kernel
+// trick: gather, do not merge").
 // The fused variant also adds the low-rank term s * v . B_a of every M-tile
 // whose 128 rows share one adapter a into the same accumulator (v from the
 // tensor-core shrink below); the other rows get theirs from the SGMV expand.
