@@ -273,10 +273,13 @@ int lora_layer_forward_noalloc(lora_pool *pool, int matrix, const void *x, const
  * lora_quantize_e4m3: per-row quantisation of x (T x h bf16, device, h a
  * multiple of 8) to e4m3 codes q (T x h bytes, device, 8-byte aligned) and
  * fp32 scales sx (T, device):
- *   sx[t] = max_k |x[t][k]| / 448  (fp32 division; 1 for a row of zeros),
- *   q[t][k] = e4m3(x[t][k] / sx[t])  (fp32 division; round to nearest even,
- *             saturating at +-448; e4m3 = 1 sign, 4 exponent bits with bias
- *             7, 3 mantissa bits, no infinities).
+ *   a = max_k |x[t][k]|, sx[t] = a / 448 and r = 448 / a (two fp32
+ *             divisions per row),
+ *   q[t][k] = e4m3(x[t][k] * r)  (the product in fp32, then rounded to the
+ *             nearest e4m3 value, ties to the even code, saturating at +-448;
+ *             e4m3 = 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *             infinities);
+ *   a row with a < 2^-120 (a row of zeros included) gets sx[t] = 1 and +0 codes.
  * Errors: LORA_ERR_ARG.
  */
 int lora_quantize_e4m3(const void *x, int T, int h, void *q, float *sx, lora_stream stream);
