@@ -250,6 +250,24 @@ class Runner:
     def secondary(self):
         return {}
 
+    def _fan(self, stream, jobs):
+        """Run independent jobs (functions of a stream) on streams of their own,
+        forked from and joined back to `stream` (the current stream if None)."""
+        torch = self.torch
+        cur = stream if stream is not None else torch.cuda.current_stream()
+        if len(getattr(self, "_fan_streams", ())) < len(jobs):
+            self._fan_streams = [torch.cuda.Stream() for _ in jobs]
+            self._fan_done = [torch.cuda.Event() for _ in jobs]
+            self._fan_fork = torch.cuda.Event()
+        self._fan_fork.record(cur)
+        for i, job in enumerate(jobs):
+            s = self._fan_streams[i]
+            s.wait_event(self._fan_fork)
+            job(s)
+            self._fan_done[i].record(s)
+        for i in range(len(jobs)):
+            cur.wait_event(self._fan_done[i])
+
 
 class DecodeBGMV(Runner):
     name = "decode_bgmv"
@@ -332,7 +350,8 @@ class PrefillSGMV(Runner):
     @staticmethod
     def describe(layers: int = 32) -> str:
         return ("prefill_sgmv: 8192 tokens in 16 Zipf(1.2) segments (cap 2048), 16 of 64 adapters, q/o 4096->4096, "
-                "k/v 4096->1024, rank 16, bf16; step = shrink+expand on q,k,v,o")
+                "k/v 4096->1024, rank 16, bf16; step = shrink+expand on q,k,v,o, the four independent projections "
+                "on four streams")
 
     def __init__(self, seed: int = 0):
         import torch
@@ -362,11 +381,15 @@ class PrefillSGMV(Runner):
 
     def step(self, stream=None):
         w, L = self.w, self.L
-        for m in range(4):
-            L.lora_sgmv_shrink(self.pool.handle, m, self._x(m), self.v[m], w.max_rank, self.ss, self.sa, w.S, w.T,
-                               stream)
-            L.lora_sgmv_expand(self.pool.handle, m, self.v[m], w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T,
-                               stream)
+
+        def proj(m):
+            def run(s):
+                L.lora_sgmv_shrink(self.pool.handle, m, self._x(m), self.v[m], w.max_rank, self.ss, self.sa, w.S,
+                                   w.T, s)
+                L.lora_sgmv_expand(self.pool.handle, m, self.v[m], w.max_rank, self.y[m], self.ss, self.sa, w.S,
+                                   w.T, s)
+            return run
+        self._fan(stream, [proj(m) for m in range(4)])
 
     def dominant_step(self, stream=None):
         w, L = self.w, self.L
@@ -429,7 +452,8 @@ class EncoderMixedRank(Runner):
     def describe(layers: int = 32) -> str:
         return ("encoder_mixed_rank: 128 sequences x 128 tokens, Zipf(1.1) ids over 1024 adapters with ranks "
                 "{8,16,32,64} (p .4/.3/.2/.1), 12 layers x q/k/v/o 768->768, pages of 768, bf16; step = "
-                "shrink+expand on 48 projections")
+                "shrink+expand on 48 projections, a layer's four independent projections on four streams, "
+                "layers in sequence")
 
     def __init__(self, seed: int = 0):
         import torch
@@ -443,7 +467,8 @@ class EncoderMixedRank(Runner):
         self.ss, self.sa = H.int_tensor(w.seg_starts), H.int_tensor(w.seg_adapter)
         self.x = [H.to_device(w.x(m), w.dtype) for m in range(self.M)]
         self.y = [H.to_device(w.y0(m), w.dtype) for m in range(self.M)]
-        self.v = torch.zeros((w.T, w.max_rank), dtype=torch.float32, device="cuda")
+        self.vs = [torch.zeros((w.T, w.max_rank), dtype=torch.float32, device="cuda") for _ in range(4)]
+        self.v = self.vs[0]
         self.units_per_step = self.T * self.M
         tok = np.repeat(w.seg_adapter, np.diff(w.seg_starts))
         eb = A.expand_bytes(tok, w.ranks, 768, 2)
@@ -458,9 +483,14 @@ class EncoderMixedRank(Runner):
 
     def step(self, stream=None):
         w, L = self.w, self.L
-        for m in range(self.M):
-            L.lora_sgmv_shrink(self.pool.handle, m, self.x[m], self.v, w.max_rank, self.ss, self.sa, w.S, w.T, stream)
-            L.lora_sgmv_expand(self.pool.handle, m, self.v, w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T, stream)
+
+        def proj(m, v):
+            def run(s):
+                L.lora_sgmv_shrink(self.pool.handle, m, self.x[m], v, w.max_rank, self.ss, self.sa, w.S, w.T, s)
+                L.lora_sgmv_expand(self.pool.handle, m, v, w.max_rank, self.y[m], self.ss, self.sa, w.S, w.T, s)
+            return run
+        for layer in range(0, self.M, 4):
+            self._fan(stream, [proj(m, self.vs[m - layer]) for m in range(layer, min(self.M, layer + 4))])
 
     def dominant_step(self, stream=None):
         w, L = self.w, self.L
