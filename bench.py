@@ -250,6 +250,69 @@ class Runner:
     def secondary(self):
         return {}
 
+    # ---- pipelined end-to-end steps ------------------------------------------
+    # Every e2e step copies its inputs in from pinned host memory and its results
+    # back; with two device buffer sets and a copy stream per tensor, step i's
+    # kernels overlap step i+1's uploads and step i-1's downloads.
+    def _pipe_init(self, dev, uploads, downloads, copy_streams: int = 4):
+        """dev: name -> device tensor (the first buffer set); uploads: name -> pinned
+        host tensor copied into it every step; downloads: name -> pinned host tensor
+        it is copied back into every step (a name may be in both).  Copies go round
+        robin over `copy_streams` streams per direction."""
+        torch = self.torch
+        self._p_dev = [dict(dev), {k: torch.empty_like(v) for k, v in dev.items()}]
+        self._p_up, self._p_down = uploads, downloads
+        cin = [torch.cuda.Stream() for _ in range(min(copy_streams, max(1, len(uploads))))]
+        cout = [torch.cuda.Stream() for _ in range(min(copy_streams, max(1, len(downloads))))]
+        self._p_cin = {k: cin[i % len(cin)] for i, k in enumerate(uploads)}
+        self._p_cout = {k: cout[i % len(cout)] for i, k in enumerate(downloads)}
+        self._p_free = [{}, {}]     # set b: name -> events after which its tensor may be overwritten
+        self._p_i = 0
+        self.h2d = sum(t.numel() * t.element_size() for t in uploads.values())
+        self.d2h = sum(t.numel() * t.element_size() for t in downloads.values())
+
+    def _pipe_step(self, jobs):
+        """jobs: (stream, fn(device tensors of this step's set, stream), reads, writes,
+        after: indices of earlier jobs of this step it must follow)."""
+        torch = self.torch
+        b = self._p_i % 2
+        self._p_i += 1
+        dev, free = self._p_dev[b], self._p_free[b]
+        up_ev = {}
+        for k, c in self._p_cin.items():
+            with torch.cuda.stream(c):
+                for e in free.get(k, ()):
+                    c.wait_event(e)
+                dev[k].copy_(self._p_up[k], non_blocking=True)
+                up_ev[k] = torch.cuda.Event()
+                up_ev[k].record(c)
+        new_free, ends = {}, []
+        for s, fn, reads, writes, after in jobs:
+            for k in set(reads) | set(writes):
+                if k in up_ev:
+                    s.wait_event(up_ev[k])
+                else:
+                    for e in free.get(k, ()):
+                        s.wait_event(e)
+            for j in after:
+                s.wait_event(ends[j])
+            fn(dev, s)
+            end = torch.cuda.Event()
+            end.record(s)
+            ends.append(end)
+            for k in set(reads) | set(writes):
+                new_free.setdefault(k, []).append(end)
+            for k in writes:
+                if k in self._p_cout:
+                    c = self._p_cout[k]
+                    with torch.cuda.stream(c):
+                        c.wait_event(end)
+                        self._p_down[k].copy_(dev[k], non_blocking=True)
+                        done = torch.cuda.Event()
+                        done.record(c)
+                    new_free[k].append(done)
+        self._p_free[b] = new_free
+
     def _fan(self, stream, jobs):
         """Run independent jobs (functions of a stream) on streams of their own,
         forked from and joined back to `stream` (the current stream if None)."""
@@ -305,22 +368,19 @@ class DecodeBGMV(Runner):
         for l in range(self.layers):
             self.L.lora_bgmv(self.pool.handle, l, self.x[l], self.y[l], self.tok, self.T, stream)
 
-    # end to end: inputs from pinned host memory, result back to pinned memory
+    # end to end: inputs from pinned host memory, result back to pinned memory (pipelined steps)
     def e2e_setup(self):
         torch = self.torch
-        self.x_h = self.x.cpu().pin_memory()
-        self.y0_h = self.y.cpu().pin_memory()
-        self.tok_h = self.tok.cpu().pin_memory()
-        self.out_h = torch.empty_like(self.y0_h).pin_memory()
-        self.h2d = self.x_h.numel() * 2 + self.y0_h.numel() * 2 + self.tok_h.numel() * 4
-        self.d2h = self.out_h.numel() * 2
+        ups = {"x": self.x.cpu().pin_memory(), "y": self.y.cpu().pin_memory(), "tok": self.tok.cpu().pin_memory()}
+        self._pipe_init({"x": self.x, "y": self.y, "tok": self.tok}, ups,
+                        {"y": torch.empty_like(ups["y"]).pin_memory()})
+        self._e2e_stream = torch.cuda.Stream()
 
     def e2e_step(self):
-        self.x.copy_(self.x_h, non_blocking=True)
-        self.y.copy_(self.y0_h, non_blocking=True)
-        self.tok.copy_(self.tok_h, non_blocking=True)
-        self.step()
-        self.out_h.copy_(self.y, non_blocking=True)
+        def run(d, s):
+            for l in range(self.layers):
+                self.L.lora_bgmv(self.pool.handle, l, d["x"][l], d["y"][l], d["tok"], self.T, s)
+        self._pipe_step([(self._e2e_stream, run, ["x", "tok"], ["y"], [])])
 
     def cpu_sample(self, budget_s: float):
         import oracle
@@ -409,20 +469,23 @@ class PrefillSGMV(Runner):
         return {"shrink_roofline": (spec, self.shrink_step)}
 
     def e2e_setup(self):
-        self.x_h = {k: v.cpu().pin_memory() for k, v in self.x.items()}
-        self.y_h = [y.cpu().pin_memory() for y in self.y]
-        self.out_h = [self.torch.empty_like(y).pin_memory() for y in self.y_h]
-        self.h2d = sum(t.numel() * 2 for t in self.x_h.values()) + sum(t.numel() * 2 for t in self.y_h)
-        self.d2h = sum(t.numel() * 2 for t in self.out_h)
+        torch = self.torch
+        dev = {"x0": self.x[0], "x3": self.x[3], **{f"y{m}": self.y[m] for m in range(4)}}
+        ups = {k: v.cpu().pin_memory() for k, v in dev.items()}
+        self._pipe_init(dev, ups, {f"y{m}": torch.empty_like(ups[f"y{m}"]).pin_memory() for m in range(4)})
+        self._e2e_streams = [torch.cuda.Stream() for _ in range(4)]
 
     def e2e_step(self):
-        for k in self.x:
-            self.x[k].copy_(self.x_h[k], non_blocking=True)
-        for y, yh in zip(self.y, self.y_h):
-            y.copy_(yh, non_blocking=True)
-        self.step()
-        for o, y in zip(self.out_h, self.y):
-            o.copy_(y, non_blocking=True)
+        w, L = self.w, self.L
+
+        def job(m):
+            xk, yk = ("x0" if m < 3 else "x3"), f"y{m}"
+
+            def run(d, s):
+                L.lora_sgmv_shrink(self.pool.handle, m, d[xk], self.v[m], w.max_rank, self.ss, self.sa, w.S, w.T, s)
+                L.lora_sgmv_expand(self.pool.handle, m, self.v[m], w.max_rank, d[yk], self.ss, self.sa, w.S, w.T, s)
+            return (self._e2e_streams[m], run, [xk], [yk], [])
+        self._pipe_step([job(m) for m in range(4)])
 
     def cpu_sample(self, budget_s: float):
         import oracle
@@ -508,18 +571,26 @@ class EncoderMixedRank(Runner):
         return {"shrink_roofline": (spec, self.shrink_step)}
 
     def e2e_setup(self):
-        self.x_h = [t.cpu().pin_memory() for t in self.x]
-        self.y_h = [t.cpu().pin_memory() for t in self.y]
-        self.out_h = [self.torch.empty_like(t).pin_memory() for t in self.y_h]
-        self.h2d = sum(t.numel() * 2 for t in self.x_h + self.y_h)
-        self.d2h = sum(t.numel() * 2 for t in self.out_h)
+        torch = self.torch
+        dev = {**{f"x{m}": self.x[m] for m in range(self.M)}, **{f"y{m}": self.y[m] for m in range(self.M)}}
+        ups = {k: v.cpu().pin_memory() for k, v in dev.items()}
+        self._pipe_init(dev, ups, {f"y{m}": torch.empty_like(ups[f"y{m}"]).pin_memory() for m in range(self.M)})
+        self._e2e_streams = [torch.cuda.Stream() for _ in range(4)]
 
     def e2e_step(self):
-        for d, h in zip(self.x + self.y, self.x_h + self.y_h):
-            d.copy_(h, non_blocking=True)
-        self.step()
-        for o, y in zip(self.out_h, self.y):
-            o.copy_(y, non_blocking=True)
+        w, L = self.w, self.L
+        jobs = []
+        for m in range(self.M):
+            layer0 = m - m % 4
+            v = self.vs[m % 4]
+
+            def run(d, s, m=m, v=v):
+                L.lora_sgmv_shrink(self.pool.handle, m, d[f"x{m}"], v, w.max_rank, self.ss, self.sa, w.S, w.T, s)
+                L.lora_sgmv_expand(self.pool.handle, m, v, w.max_rank, d[f"y{m}"], self.ss, self.sa, w.S, w.T, s)
+            # the layers in sequence: a projection follows every projection of the layer before
+            after = list(range(layer0 - 4, layer0)) if layer0 >= 4 else []
+            jobs.append((self._e2e_streams[m % 4], run, [f"x{m}"], [f"y{m}"], after))
+        self._pipe_step(jobs)
 
     def cpu_sample(self, budget_s: float):
         import oracle
@@ -589,10 +660,11 @@ class FusedLayer(Runner):
         self.fork = torch.cuda.Event()
         self.done = [torch.cuda.Event() for _ in range(4)]
 
-    def _call(self, m, stream):
+    def _call(self, m, stream, x=None, y=None):
         w = self.w
-        self.L.lora_layer_forward(self.pool.handle, m, self._x(m), self.W[m], self.y[m], self.ss, self.sa, w.S, w.T,
-                                  self.wss[m], self.ws_bytes, stream)
+        self.L.lora_layer_forward(self.pool.handle, m, self._x(m) if x is None else x, self.W[m],
+                                  self.y[m] if y is None else y, self.ss, self.sa, w.S, w.T, self.wss[m],
+                                  self.ws_bytes, stream)
 
     def step(self, stream=None):
         cur = stream if stream is not None else self.torch.cuda.current_stream()
@@ -605,17 +677,17 @@ class FusedLayer(Runner):
             cur.wait_event(self.done[m])
 
     def e2e_setup(self):
-        self.x_h = {k: v.cpu().pin_memory() for k, v in self.x.items()}
-        self.out_h = [self.torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in self.y]
-        self.h2d = sum(t.numel() * 2 for t in self.x_h.values())
-        self.d2h = sum(t.numel() * 2 for t in self.out_h)
+        torch = self.torch
+        dev = {"x0": self.x[0], "x3": self.x[3], **{f"y{m}": self.y[m] for m in range(4)}}
+        ups = {"x0": self.x[0].cpu().pin_memory(), "x3": self.x[3].cpu().pin_memory()}
+        downs = {f"y{m}": torch.empty(self.y[m].shape, dtype=self.y[m].dtype).pin_memory() for m in range(4)}
+        self._pipe_init(dev, ups, downs)
 
     def e2e_step(self):
-        for k in self.x:
-            self.x[k].copy_(self.x_h[k], non_blocking=True)
-        self.step()
-        for o, y in zip(self.out_h, self.y):
-            o.copy_(y, non_blocking=True)
+        def job(m):
+            xk, yk = ("x0" if m < 3 else "x3"), f"y{m}"
+            return (self.streams[m], lambda d, s: self._call(m, s, d[xk], d[yk]), [xk], [yk], [])
+        self._pipe_step([job(m) for m in range(4)])
 
     def cpu_sample(self, budget_s: float):
         import oracle
@@ -667,10 +739,11 @@ class FusedLayerFp8(FusedLayer):
                              peak_key="fp8")
         self.config = dict(self.config, workload=self.describe())
 
-    def _call(self, m, stream):
+    def _call(self, m, stream, x=None, y=None):
         w = self.w
-        self.L.lora_layer_forward_fp8(self.pool.handle, m, self._x(m), self.W8[m], self.s_w[m], self.y[m], self.ss,
-                                      self.sa, w.S, w.T, self.wss[m], self.ws_bytes, stream)
+        self.L.lora_layer_forward_fp8(self.pool.handle, m, self._x(m) if x is None else x, self.W8[m], self.s_w[m],
+                                      self.y[m] if y is None else y, self.ss, self.sa, w.S, w.T, self.wss[m],
+                                      self.ws_bytes, stream)
 
     def cpu_sample(self, budget_s: float):
         import oracle
