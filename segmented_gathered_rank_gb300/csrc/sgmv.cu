@@ -947,6 +947,7 @@ struct ExpandParams {
     int ld_v;
     __nv_bfloat16 *y;
     int ncg;       // column groups per item
+    int n_work;    // segment tables: items (upper bound) x column groups
     int bpu;       // column blocks per unit (1 .. kMaxBlocksPerUnit)
     const Unit *units;    // unit kernel: the plan's expand units (count plan[3])
 };
@@ -1257,10 +1258,14 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
                                         kStagesE * kpc * yp + 2 * kM * vp) + kM;
     int *scan = wtot + 8 + p.pv.rec_ints;
     if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
-    const int cg = blockIdx.x % p.ncg;
-    const Item it = get_item<kThreadsE>(p.src, blockIdx.x / p.ncg, scan, wtot);
-    if (it.a < 0 || it.nt <= 0) return;
-    expand_unit(p, it, 0u, cg * p.bpu, p.bpu, cg == 0, smem_raw);
+    // persistent: CTA c takes work c, c + G, ... (work = item x column group)
+    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+        __syncthreads();                          // the previous unit's readers of shared memory are done
+        const int cg = w % p.ncg;
+        const Item it = get_item<kThreadsE>(p.src, w / p.ncg, scan, wtot);
+        if (it.a < 0 || it.nt <= 0) continue;
+        expand_unit(p, it, 0u, cg * p.bpu, p.bpu, cg == 0, smem_raw);
+    }
 }
 
 // Layer plans: persistent CTAs walk the plan's expand units (costly ones first,
@@ -1489,7 +1494,11 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
     }
     p.units = nullptr;
     const int groups = plan ? std::max(1, pool->mat_n_ids[matrix]) : S;
-    sgmv_expand_kernel<<<item_bound(groups, T) * p.ncg, kThreadsE, smem, st>>>(p);
+    p.n_work = item_bound(groups, T) * p.ncg;
+    int occ = 0;
+    if (smem_optin(reinterpret_cast<const void *>(sgmv_expand_kernel), smem, kThreadsE, &occ)) return LORA_ERR_CUDA;
+    const int grid = std::max(1, std::min(p.n_work, num_sms() * std::max(1, occ)));
+    sgmv_expand_kernel<<<grid, kThreadsE, smem, st>>>(p);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
