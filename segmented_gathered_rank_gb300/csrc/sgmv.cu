@@ -45,7 +45,7 @@ constexpr int kRowsS = 16;        // rows per 128-thread shrink CTA (half an ite
 constexpr int kStagesS = 4;
 constexpr int kNb = 128;          // output columns per expand block
 constexpr int kMaxBlocksPerUnit = 8; // column blocks per expand unit (up to 1024 columns)
-constexpr int kStagesE = 4;
+constexpr int kStagesE = 2;      // expand ring depth: shallow rings leave room for more CTAs per SM
 constexpr int kMaxS = 8192;       // segments the segment-mode kernels take
 constexpr int kPlanThreads = 1024;
 constexpr int kTileRows = kFuseTileRows;   // M-tile rows of the tensor-core GEMM
