@@ -6,8 +6,8 @@
 //   expand:  y[t][n] += s_a * sum_j v[t][j] * B_a[j][n]
 //
 // Work items are one adapter and up to kM of its tokens.  They come either
-// from the segment table (each segment cut into kM-token chunks; every CTA
-// finds its item with a block-wide scan of chunk counts and a binary search,
+// from the segment table (each segment cut into kM-token chunks; a CTA finds
+// each of its items with a block-wide scan of chunk counts and a binary search,
 // so Zipf-skewed segment lengths spread over as many CTAs as they have
 // chunks), or from a plan built by sgmv_plan_kernel, which groups the tokens
 // of a batch by adapter with a counting sort (so a decode batch whose tokens
@@ -16,8 +16,9 @@
 // For the adapted layer the plan also marks the GEMM M-tiles whose rows share
 // one adapter (the GEMM adds their term itself) and lists, for the items that
 // keep other rows, work units ordered by cost: shrink units (a 16-row half x
-// a 32-rank chunk) and expand units (a range of column blocks, narrower for
-// costly items).  Persistent kernels walk these lists in snake order, the
+// a 32-rank chunk) and expand units (a range of column blocks, sized so that
+// the batch's units fill the resident CTAs about once).  Persistent kernels
+// walk these lists in snake order, the
 // shrink as clusters of two CTAs that split K and add their partial sums
 // through distributed shared memory.
 //
@@ -1483,7 +1484,7 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
     if (smem_optin(reinterpret_cast<const void *>(sgmv_expand_kernel), smem)) return LORA_ERR_CUDA;
     if (tile_ad && plan) {
         // layer plan: persistent CTAs over the plan's expand units, in passes of at most 32
-        // ranks (a third CTA per SM; only units of ranks above 32 take more passes)
+        // ranks (a smaller CTA, so more fit per SM; only units of ranks above 32 take more passes)
         p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).eu);
         p.kpc = expand_units_kpc(pool);
         const int grid = expand_units_grid(pool);
