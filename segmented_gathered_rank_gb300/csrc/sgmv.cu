@@ -236,6 +236,13 @@ __device__ __forceinline__ const Item *plan_items(const int *plan, int T) {
     return reinterpret_cast<const Item *>(plan + 4 + ((T + 3) & ~3));
 }
 
+// Entry i of a plan's token permutation, i clamped into [0, T) (a plan is
+// read only after its kernel wrote it; the clamp keeps a damaged workspace
+// from sending a read outside the plan).
+__device__ __forceinline__ int perm_at(const ItemSource &src, int i) {
+    return plan_perm(src.plan)[min(max(i, 0), src.T - 1)];
+}
+
 template <int NT>
 __device__ Item get_item(const ItemSource &src, int idx, int *scan, int *wtot) {
     if (src.plan) return plan_items(src.plan, src.T)[idx];   // idx < the plan's item bound; unused items have a = -1
@@ -531,6 +538,8 @@ struct ShrinkParams {
     float *v;
     int ld_v;
     const Unit *units;   // unit kernel: the plan's shrink units (count plan[2])
+    int max_units;       // unit kernel: the plan's room for shrink units
+    int n_work, n_chunks;   // wide kernel: (item, rank chunk) work entries; rank chunks per item
 };
 
 // Rows tok[0 .. nt) of x, K stages kc0 .. kc1-1, times ranks j0 .. j0+np-1 of the
@@ -667,7 +676,7 @@ __global__ void __launch_bounds__(kThreadsS, 4) sgmv_shrink_kernel(ShrinkParams 
     if (it.a < 0 || nt <= 0) return;
     // the item's tokens load together with the record (load_record's barrier publishes both)
     if (tid < kRowsS)
-        tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + row0 + tid] : it.off + row0 + tid, 0),
+        tok[tid] = tid < nt ? min(max(p.src.plan ? perm_at(p.src, it.off + row0 + tid) : it.off + row0 + tid, 0),
                                   p.src.T - 1)
                             : 0;
     if (!load_record<kThreadsS>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0 && blockIdx.z == 0)) return;
@@ -716,7 +725,7 @@ __global__ void __launch_bounds__(kThreadsS, 3) sgmv_shrink_units_kernel(ShrinkP
 
     cg::cluster_group cl = cg::this_cluster();
     const int ks = (int)cl.num_blocks(), kpart = (int)cl.block_rank();
-    const int n_units = p.src.plan[2];
+    const int n_units = min(max(p.src.plan[2], 0), p.max_units);
     const int G = gridDim.y, c = blockIdx.y;
     const int nk = p.h_in / kKs;
     const int kc0 = kpart * nk / ks, kc1 = (kpart + 1) * nk / ks;
@@ -726,11 +735,11 @@ __global__ void __launch_bounds__(kThreadsS, 3) sgmv_shrink_units_kernel(ShrinkP
         const int u = k * G + ((k & 1) ? G - 1 - c : c);
         if (u >= n_units) break;                  // the same for every CTA of the cluster
         const Unit un = p.units[u];
-        const int row0 = ((un.info >> 6) & 1) * kRowsS, chunk = un.info >> 8;
+        const int row0 = ((un.info >> 6) & 1) * kRowsS, chunk = (int)((unsigned)un.info >> 8);
         const int nt = min(kRowsS, (un.info & 63) - row0);
         __syncthreads();                          // the previous unit's readers of tok and rec are done
         if (tid < kRowsS)
-            tok[tid] = tid < nt ? min(max(plan_perm(p.src.plan)[un.off + row0 + tid], 0), p.src.T - 1) : 0;
+            tok[tid] = tid < nt ? min(max(perm_at(p.src, un.off + row0 + tid), 0), p.src.T - 1) : 0;
         if (!load_record<kThreadsS>(p.pv, un.a, p.m, rec, false)) continue;
         const int r = min(rec[0], min(p.pv.max_rank, p.ld_v));
         const int j0 = chunk * npc;
@@ -775,8 +784,8 @@ constexpr int kThreadsW = 256;
 constexpr int kRowsW = kM;
 constexpr int kStagesW = 4;
 
-__global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+// One work entry of the wide shrink: item bx, rank chunk by.
+__device__ __forceinline__ void shrink_wide_item(const ShrinkParams &p, const int bx, const int by, uint8_t *smem_raw) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int pitch = kKs + 8;                                        // bf16 per smem row
     const int npc = p.npc;
@@ -788,12 +797,11 @@ __global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkPa
     int *scan = reinterpret_cast<int *>(smem_raw);                       // [S + 1], before the pipeline starts
     float *red = reinterpret_cast<float *>(smem_raw);                    // [3][32][npc], after it ends
 
-    if (blockIdx.x == 0 && blockIdx.y == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
-    const Item it = get_item<kThreadsW>(p.src, blockIdx.x, scan, wtot);
+    const Item it = get_item<kThreadsW>(p.src, bx, scan, wtot);
     const int nt = min(kRowsW, it.nt);
     if (it.a < 0 || nt <= 0) return;
     if (tid < kRowsW)
-        tok[tid] = tid < nt ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + tid] : it.off + tid, 0), p.src.T - 1)
+        tok[tid] = tid < nt ? min(max(p.src.plan ? perm_at(p.src, it.off + tid) : it.off + tid, 0), p.src.T - 1)
                             : 0;
     // x rows past the item stay zero
     for (int i = tid; i < kStagesW * kRowsW * (pitch / 8); i += kThreadsW)
@@ -823,13 +831,13 @@ __global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkPa
     for (int kc = 0; kc < kStagesW - 1; ++kc)
         if (kc < nk) issue_x(kc);
 
-    const bool ok = load_record<kThreadsW>(p.pv, it.a, p.m, rec, tid == 0 && blockIdx.y == 0);
+    const bool ok = load_record<kThreadsW>(p.pv, it.a, p.m, rec, tid == 0 && by == 0);
     bool skip = !ok;
     if (ok && p.tc_min_rows > 0 && !p.src.plan && it.pad >= p.tc_min_rows && rec[0] >= kShrinkTcSegMinRank &&
         rec[0] <= kFuseMaxRank && rec[0] <= p.ld_v)
         skip = true;                             // the tensor-core shrink computed this segment
     const int r = ok ? min(rec[0], min(p.pv.max_rank, p.ld_v)) : 0;
-    const int j0 = blockIdx.y * npc;
+    const int j0 = by * npc;
     if (skip || j0 >= r) {
         cp_commit();       // nothing may be in flight into shared memory when the CTA exits
         cp_wait<0>();
@@ -931,6 +939,16 @@ __global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkPa
     }
 }
 
+// Persistent over (item, rank chunk) work entries: CTA c takes c, c + G, ...
+__global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+        __syncthreads();                          // the previous entry's readers of shared memory are done
+        shrink_wide_item(p, w / p.n_chunks, w % p.n_chunks, smem_raw);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Expand: 128 threads, unit = (item, up to bpu <= kMaxBlocksPerUnit column blocks of
 // kNb).  warp w: rows 16*(w & 1) .. +16, columns 64*(w >> 1) .. +64 of the
@@ -951,6 +969,7 @@ struct ExpandParams {
     int n_work;    // segment tables: items (upper bound) x column groups
     int bpu;       // column blocks per unit (1 .. kMaxBlocksPerUnit)
     const Unit *units;    // unit kernel: the plan's expand units (count plan[3])
+    int max_units;        // unit kernel: the plan's room for expand units
 };
 
 // Rows of item `it` outside `fused` x column blocks b_first .. b_first + nb_req - 1.
@@ -979,7 +998,7 @@ __device__ __forceinline__ void expand_unit(const ExpandParams &p, const Item &i
         rec[i] = p.pv.table[((long long)it.a * p.pv.n_matrices + p.m) * p.pv.rec_ints + i];
     if (warp == 0) {   // the item's tokens, minus rows whose term the GEMM already added (one per lane)
         const bool keep = lane < it.nt && !((fused >> lane) & 1u);
-        const int t = keep ? min(max(p.src.plan ? plan_perm(p.src.plan)[it.off + lane] : it.off + lane, 0),
+        const int t = keep ? min(max(p.src.plan ? perm_at(p.src, it.off + lane) : it.off + lane, 0),
                                  p.src.T - 1)
                            : 0;
         const unsigned kept = __ballot_sync(0xffffffffu, keep);
@@ -1273,7 +1292,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
 // snake order: CTA c takes units c, 2G - 1 - c, 2G + c, ...).
 __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_units_kernel(ExpandParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    const int n_units = p.src.plan[3];
+    const int n_units = min(max(p.src.plan[3], 0), p.max_units);
     const int G = gridDim.x, c = blockIdx.x;
     for (int k = 0;; ++k) {
         const int u = k * G + ((k & 1) ? G - 1 - c : c);
@@ -1281,7 +1300,7 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_units_kernel(ExpandP
         const Unit un = p.units[u];
         __syncthreads();                          // the previous unit's readers of shared memory are done
         const Item it{un.a, un.off, un.info & 63, un.pad};
-        expand_unit(p, it, (unsigned)un.pad, un.info >> 10, (un.info >> 6) & 15, false, smem_raw);
+        expand_unit(p, it, (unsigned)un.pad, (int)((unsigned)un.info >> 10), (un.info >> 6) & 15, false, smem_raw);
     }
 }
 
@@ -1411,6 +1430,7 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
         p.npc = shrink_npc(pool);
         p.alias_bytes = 0;
         p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).su);
+        p.max_units = plan_layout(pool, matrix, T).max_su;
         const size_t smem = (size_t)kStagesS * (kRowsS + p.npc) * (kKs + 8) * 2 + (size_t)4 * 16 * p.npc * 4 +
                             (size_t)(kRowsS + p.pv.rec_ints) * 4 + 16;
         int occ = 0;
@@ -1445,8 +1465,12 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
                              ~(size_t)15;
         p.alias_bytes = (int)alias;
         const size_t smem_w = alias + (size_t)(kRowsW + kThreadsW / 32 + 4 + p.pv.rec_ints) * 4;
-        if (smem_optin(reinterpret_cast<const void *>(sgmv_shrink_wide_kernel), smem_w)) return LORA_ERR_CUDA;
-        const dim3 grid_w(item_bound(groups, T), (pool->max_rank + p.npc - 1) / p.npc, 1);
+        int occ = 0;
+        if (smem_optin(reinterpret_cast<const void *>(sgmv_shrink_wide_kernel), smem_w, kThreadsW, &occ))
+            return LORA_ERR_CUDA;
+        p.n_chunks = (pool->max_rank + p.npc - 1) / p.npc;
+        p.n_work = item_bound(groups, T) * p.n_chunks;
+        const int grid_w = std::max(1, std::min(p.n_work, num_sms() * std::max(1, occ)));
         sgmv_shrink_wide_kernel<<<grid_w, kThreadsW, smem_w, st>>>(p);
         count_launch();
         return cuda_status(cudaGetLastError());
@@ -1486,6 +1510,7 @@ int launch_sgmv_expand(const lora_pool *pool, int matrix, int h_out, const float
         // layer plan: persistent CTAs over the plan's expand units, in passes of at most 32
         // ranks (a smaller CTA, so more fit per SM; only units of ranks above 32 take more passes)
         p.units = reinterpret_cast<const Unit *>(plan + plan_layout(pool, matrix, T).eu);
+        p.max_units = plan_layout(pool, matrix, T).max_eu;
         p.kpc = expand_units_kpc(pool);
         const int grid = expand_units_grid(pool);
         if (grid <= 0) return LORA_ERR_CUDA;

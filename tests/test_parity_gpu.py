@@ -429,8 +429,9 @@ def test_fused_layer_bit_identical_across_calls_and_streams():
         Ws = [H.to_device(w.W(m), w.dtype) for m in range(4)]
         ws_bytes = max(L.lora_layer_forward_workspace_size(dp.handle, m, w.S, w.T) for m in range(4))
 
-        def call(m, y, fill, stream=None):
-            ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device="cuda")
+        def call(m, y, fill, stream=None, ws=None):
+            if ws is None:
+                ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device="cuda")
             L.lora_layer_forward(dp.handle, m, xs[0 if m < 3 else 3], Ws[m], y, ss, sa, w.S, w.T, ws, stream=stream)
             return ws
 
@@ -452,12 +453,13 @@ def test_fused_layer_bit_identical_across_calls_and_streams():
                 assert torch.equal(y, ref[m]), (fill, m)
         streams = [torch.cuda.Stream() for _ in range(4)]
         ys = [new_y(m) for m in range(4)]
+        # every buffer is filled before the event the four streams wait on
+        wss = [torch.full((ws_bytes,), 0x7f, dtype=torch.uint8, device="cuda") for _ in range(4)]
         start = torch.cuda.Event()
         start.record()
-        keep = []
         for m in range(4):
             streams[m].wait_event(start)
-            keep.append(call(m, ys[m], 0x7f, streams[m]))
+            call(m, ys[m], None, streams[m], wss[m])
         torch.cuda.synchronize()
         for m in range(4):
             assert torch.equal(ys[m], ref[m]), m
