@@ -193,14 +193,20 @@ struct Unit {
 // Item `idx` among the (segment, kM-token chunk) pairs of a segment table.
 // scan: S + 1 ints of shared memory; wtot: NT/32 + 4 ints.  All threads return it.
 template <int NT>
-__device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int S, int T, int idx, int *scan,
-                             int *wtot) {
+__device__ int segment_scan(const int *seg_starts, int S, int T, int *scan, int *wtot) {
     for (int s = threadIdx.x; s < S; s += NT) {
         const int a = min(max(seg_starts[s], 0), T), b = min(max(seg_starts[s + 1], 0), T);
         scan[s] = b > a ? (b - a + kM - 1) / kM : 0;
     }
     __syncthreads();
-    const int total = block_scan<NT>(scan, S, wtot);
+    return block_scan<NT>(scan, S, wtot);
+}
+
+// Item idx from a chunk scan made by segment_scan (total: its chunk count).
+// All threads call it and return the item.
+template <int NT>
+__device__ Item segment_lookup(const int *seg_starts, const int *seg_adapter, int S, int T, int idx,
+                               const int *scan, int total, int *wtot) {
     if (threadIdx.x == 0) {
         Item it{-1, 0, 0, 0};
         if (idx < total) {
@@ -222,6 +228,13 @@ __device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int 
     const Item it = reinterpret_cast<Item *>(wtot)[0];
     __syncthreads();
     return it;
+}
+
+template <int NT>
+__device__ Item segment_item(const int *seg_starts, const int *seg_adapter, int S, int T, int idx, int *scan,
+                             int *wtot) {
+    const int total = segment_scan<NT>(seg_starts, S, T, scan, wtot);
+    return segment_lookup<NT>(seg_starts, seg_adapter, S, T, idx, scan, total, wtot);
 }
 
 // The work items of one launch: from a plan (if given) or from the segment table.
@@ -1278,11 +1291,15 @@ __global__ void __launch_bounds__(kThreadsE, 4) sgmv_expand_kernel(ExpandParams 
                                         kStagesE * kpc * yp + 2 * kM * vp) + kM;
     int *scan = wtot + 8 + p.pv.rec_ints;
     if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
-    // persistent: CTA c takes work c, c + G, ... (work = item x column group)
+    // persistent: CTA c takes work c, c + G, ... (work = item x column group); a
+    // segment table's chunk scan is made once and kept (it is the same for every item)
+    const int total = p.src.plan ? 0 : segment_scan<kThreadsE>(p.src.seg_starts, p.src.S, p.src.T, scan, wtot);
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
         __syncthreads();                          // the previous unit's readers of shared memory are done
         const int cg = w % p.ncg;
-        const Item it = get_item<kThreadsE>(p.src, w / p.ncg, scan, wtot);
+        const Item it = p.src.plan ? plan_items(p.src.plan, p.src.T)[w / p.ncg]
+                                   : segment_lookup<kThreadsE>(p.src.seg_starts, p.src.seg_adapter, p.src.S, p.src.T,
+                                                               w / p.ncg, scan, total, wtot);
         if (it.a < 0 || it.nt <= 0) continue;
         expand_unit(p, it, 0u, cg * p.bpu, p.bpu, cg == 0, smem_raw);
     }
