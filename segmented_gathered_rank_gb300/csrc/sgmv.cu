@@ -797,8 +797,8 @@ constexpr int kThreadsW = 256;
 constexpr int kRowsW = kM;
 constexpr int kStagesW = 4;
 
-// One work entry of the wide shrink: item bx, rank chunk by.
-__device__ __forceinline__ void shrink_wide_item(const ShrinkParams &p, const int bx, const int by, uint8_t *smem_raw) {
+// One work entry of the wide shrink: item it, rank chunk by.
+__device__ __forceinline__ void shrink_wide_item(const ShrinkParams &p, const Item &it, const int by, uint8_t *smem_raw) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int pitch = kKs + 8;                                        // bf16 per smem row
     const int npc = p.npc;
@@ -807,10 +807,8 @@ __device__ __forceinline__ void shrink_wide_item(const ShrinkParams &p, const in
     int *tok = reinterpret_cast<int *>(smem_raw + p.alias_bytes);         // [32]
     int *wtot = tok + kRowsW;                                            // [kThreadsW / 32 + 4]
     int *rec = wtot + kThreadsW / 32 + 4;                                // [rec_ints]
-    int *scan = reinterpret_cast<int *>(smem_raw);                       // [S + 1], before the pipeline starts
     float *red = reinterpret_cast<float *>(smem_raw);                    // [3][32][npc], after it ends
 
-    const Item it = get_item<kThreadsW>(p.src, bx, scan, wtot);
     const int nt = min(kRowsW, it.nt);
     if (it.a < 0 || nt <= 0) return;
     if (tid < kRowsW)
@@ -956,9 +954,17 @@ __device__ __forceinline__ void shrink_wide_item(const ShrinkParams &p, const in
 __global__ void __launch_bounds__(kThreadsW, 2) sgmv_shrink_wide_kernel(ShrinkParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     if (blockIdx.x == 0 && !p.src.plan) check_segments(p.src.seg_starts, p.src.S, p.src.T, p.pv.status);
+    // a segment table's chunk scan, made once (it is the same for every item), after the rest
+    int *wtot = reinterpret_cast<int *>(smem_raw + p.alias_bytes) + kRowsW;
+    int *scan = wtot + kThreadsW / 32 + 4 + p.pv.rec_ints;
+    const int total = p.src.plan ? 0 : segment_scan<kThreadsW>(p.src.seg_starts, p.src.S, p.src.T, scan, wtot);
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
         __syncthreads();                          // the previous entry's readers of shared memory are done
-        shrink_wide_item(p, w / p.n_chunks, w % p.n_chunks, smem_raw);
+        const int idx = w / p.n_chunks;
+        const Item it = p.src.plan ? plan_items(p.src.plan, p.src.T)[idx]
+                                   : segment_lookup<kThreadsW>(p.src.seg_starts, p.src.seg_adapter, p.src.S, p.src.T,
+                                                               idx, scan, total, wtot);
+        shrink_wide_item(p, it, w % p.n_chunks, smem_raw);
     }
 }
 
@@ -1478,10 +1484,9 @@ int launch_sgmv_shrink(const lora_pool *pool, int matrix, int h_in, const void *
         p.npc = std::min(64, (pool->max_rank + 15) / 16 * 16);
         constexpr int pitch = kKs + 8;
         const size_t pipe = (size_t)kStagesW * (kRowsW + p.npc) * pitch * 2;
-        const size_t alias = (std::max({pipe, (size_t)3 * kRowsW * p.npc * 4, (size_t)(S + 1) * 4}) + 15) &
-                             ~(size_t)15;
+        const size_t alias = (std::max(pipe, (size_t)3 * kRowsW * p.npc * 4) + 15) & ~(size_t)15;
         p.alias_bytes = (int)alias;
-        const size_t smem_w = alias + (size_t)(kRowsW + kThreadsW / 32 + 4 + p.pv.rec_ints) * 4;
+        const size_t smem_w = alias + (size_t)(kRowsW + kThreadsW / 32 + 4 + p.pv.rec_ints + S + 1) * 4;
         int occ = 0;
         if (smem_optin(reinterpret_cast<const void *>(sgmv_shrink_wide_kernel), smem_w, kThreadsW, &occ))
             return LORA_ERR_CUDA;
